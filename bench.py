@@ -1,0 +1,403 @@
+#!/usr/bin/env python3
+"""Benchmark of the indexed sparse prefill path on GB300.
+
+A step is one call of dsa_prefill_chunk on the 128K-context workload: one
+4096-row chunk at absolute offset 126,976 of a 131,072-token context (31,744
+synthetic pooled rows already cached), index_topk 2048, H_I=64/d_I=128,
+H=64/D=512 bf16, window 128 -- pool/append, indexer score + top-k (full path)
+and window + selected attention. Between steps the PoolingCache counters are
+rolled back (O(1)) and L2 is flushed with a 512 MiB write outside the timed
+events. Prints one JSON line (rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+--impl reference times the CPU oracle (fp64 C, OpenMP) on a bounded sample of
+query rows of the same workload and prints the same metric for it.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "indexed-attn prefill query tok/s/layer @128K ctx; % of BF16 tensor peak"
+UNIT = "query tok/s/layer"
+WORKLOAD = "ctx_128k"
+WORKLOAD_DESC = ("one 4096-row prefill chunk at offset 126,976 of a 131,072-token context "
+                 "(31,744 prefix pooled rows -> 32,768), ratio 4, index_topk 2048, "
+                 "H_I=64 d_I=128, H=64 D=512 bf16, window 128, synthetic N(0,1)")
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        d = json.load(open(path))
+        out = {}
+        for key in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained"):
+            v = d.get(key)
+            if isinstance(v, dict):
+                v = v.get("value")
+            out[key] = float(v)
+        return out, "measured"
+    except Exception:
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+def work_counts(wl):
+    """Algorithmic work of one step: score flops, attention flops, bytes."""
+    T, off, k, W = wl.chunks[0], wl.off0, wl.index_topk, wl.window
+    n = (off + T) // 4
+    score_flops = attn_flops = 0
+    topk_bytes = 0
+    for i in range(T):
+        t = off + i
+        nv = min((t + 1) // 4, n)
+        score_flops += 2 * 64 * 128 * nv
+        topk_bytes += 4 * nv
+        attn_flops += 4 * 64 * 512 * (min(W, t + 1) + min(k, nv))
+    return {"score_flops": score_flops, "attn_flops": attn_flops,
+            "score_read_bytes": T * 64 * 128 * 2 + T * 64 * 4 + n * 128 * 2,
+            "score_write_bytes": 4 * T * ((n + 127) // 128 * 128),
+            "topk_bytes": topk_bytes + T * k * 4,
+            "pool_bytes": T * 640 * 2 + (T // 4) * 640 * 2}
+
+
+class ClockSampler:
+    """nvidia-smi clocks/throttle reasons sampled every 200 ms while running."""
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv") \
+            if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else f"/tmp/dsa_clocks_{os.getpid()}.csv"
+
+    def __enter__(self):
+        q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+        try:
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.fh, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+        time.sleep(0.3)
+        return self
+
+    def __exit__(self, *a):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if not self.proc:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                mx.append(float(f[2]))
+            except ValueError:
+                continue
+            for name, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_setup(n_gpus):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if os.environ.get("DSA_BENCH_BACKEND", "nccl") == "nccl" else "gloo"
+        dist.init_process_group(backend)
+    return rank, world
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def cpu_baseline(wl, seconds_budget: float = 20.0, max_rows: int = 256):
+    """The oracle, as it stands, on sampled query rows of the workload."""
+    import numpy as np
+    import oracle
+    from deepseek_v4_sparse_ratio_gb300 import inputs
+    T, off = wl.chunks[0], wl.off0
+    st = oracle.PoolState.from_prefix(wl.t["prefix_ik"], wl.t["prefix_kv"], off)
+    t0 = time.perf_counter()
+    st.append(wl.t["raw_ik"], wl.t["raw_kv"], off)
+    t_pool = time.perf_counter() - t0
+    raw_all = __import__("torch").cat([wl.t["prefix_win"], wl.t["raw_kv"]], 0)
+    raw_start = off - wl.t["prefix_win"].shape[0]
+    # probe the per-row cost on 8 rows, then size the sample to the budget
+    rows_done, elapsed = 0, 0.0
+    S = 8
+    while True:
+        rows = inputs.sample_rows(T, S)
+        pos = off + np.asarray(rows)
+        t0 = time.perf_counter()
+        sel, _, _ = oracle.select(oracle.as_bf16_bits(wl.t["q_idx"])[rows],
+                                  wl.t["w"].numpy()[rows], pos, st.pooled_ik, st.n_pooled, 4,
+                                  wl.index_topk)
+        oracle.attention(oracle.as_bf16_bits(wl.t["q"])[rows], pos, raw_all, raw_start,
+                         st.pooled_kv, st.n_pooled, sel, wl.window, 1 / math.sqrt(512))
+        dt = time.perf_counter() - t0
+        rows_done, elapsed = len(rows), dt
+        if S >= max_rows or dt > seconds_budget * 0.5:
+            break
+        S = min(max_rows, max(S * 2, int(S * seconds_budget / max(dt, 1e-3))))
+    # pooling is per chunk: charge its share per row
+    per_row = elapsed / rows_done + t_pool / T
+    return {"value": 1.0 / per_row, "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
+            "sample": f"{rows_done} evenly spaced query rows of the 4096-row chunk "
+                      f"(score all visible pooled rows + top-k + attention, fp64), "
+                      f"plus the chunk's pooling", "seconds": elapsed + t_pool}
+
+
+def run_reference(args):
+    """--impl reference: the CPU oracle timed as the reference arm."""
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    import numpy as np
+    import oracle
+    from deepseek_v4_sparse_ratio_gb300 import inputs
+    wl = inputs.draw(inputs.workload(WORKLOAD))
+    T, off = wl.chunks[0], wl.off0
+    oracle.build()
+    base = oracle.PoolState.from_prefix(wl.t["prefix_ik"], wl.t["prefix_kv"], off)
+    raw_all = __import__("torch").cat([wl.t["prefix_win"], wl.t["raw_kv"]], 0)
+    raw_start = off - wl.t["prefix_win"].shape[0]
+    rows_per_step = args.ref_rows
+
+    def step(i):
+        st = base.copy()
+        st.append(wl.t["raw_ik"], wl.t["raw_kv"], off)
+        rows = [(i * 997 + r * (T // rows_per_step)) % T for r in range(rows_per_step)]
+        pos = off + np.asarray(rows)
+        sel, _, _ = oracle.select(oracle.as_bf16_bits(wl.t["q_idx"])[rows],
+                                  wl.t["w"].numpy()[rows], pos, st.pooled_ik, st.n_pooled, 4,
+                                  wl.index_topk)
+        oracle.attention(oracle.as_bf16_bits(wl.t["q"])[rows], pos, raw_all, raw_start,
+                         st.pooled_kv, st.n_pooled, sel, wl.window, 1 / math.sqrt(512))
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(args.warmup + i)
+    dt = (time.perf_counter() - t0) / args.steps
+    value = rows_per_step / dt
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic",
+            "config": {"workload": WORKLOAD_DESC, "rows_per_step": rows_per_step},
+            "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.threads(),
+                             "kind": "oracle",
+                             "sample": f"{rows_per_step} query rows per step (of 4096) + the "
+                                       f"chunk's pooling"},
+            "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--workload", default=WORKLOAD)
+    ap.add_argument("--tile-rows", type=int, default=0)
+    ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--ref-rows", type=int, default=16)
+    args = ap.parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+
+    import torch
+    import deepseek_v4_sparse_ratio_gb300 as dsa
+    from deepseek_v4_sparse_ratio_gb300 import _binding as B
+    from deepseek_v4_sparse_ratio_gb300 import inputs
+    from deepseek_v4_sparse_ratio_gb300.runner import DeviceWorkload
+
+    rank, world = dist_setup(args.gpus)
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    dsa.build()
+
+    wl = inputs.workload(args.workload)
+    wl.seed += 1000 * rank   # independent replica per rank
+    inputs.draw(wl)
+    T = wl.chunks[0]
+    assert len(wl.chunks) == 1 and wl.off0 > 0, "bench workloads are single-chunk with a prefix"
+    tile = args.tile_rows or wl.tile_rows[0]
+    dw = DeviceWorkload(wl, tile_rows=tile, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(512 * 2 ** 20 // 4, dtype=torch.float32, device=dev)
+    snap = dw.state.snapshot()
+    counts = work_counts(wl)
+    n = (wl.off0 + T) // 4
+
+    def step():
+        dw.state.restore(snap)
+        dw.run_chunk(0, stream)
+
+    # ---- warm-up
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    dw.check_status()
+
+    # ---- timed steps (device events around each step; L2 flushed between)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        w0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.zero_()
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - w0
+    barrier(world)
+    dw.check_status()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    ms = max_over_ranks(sum(step_ms) / len(step_ms), world, dev)
+    value = world * T / (ms * 1e-3)
+
+    # ---- per-component times: the same calls one ABI entry point at a time
+    comp = {"pool": [], "score_topk": [], "attention": []}
+    s, off, k = 0, wl.off0, wl.index_topk
+    for i in range(max(3, args.steps // 2)):
+        flush.zero_()
+        dw.state.restore(snap)
+        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+        e[0].record(stream)
+        B.dsa_pool_append(dw.state, dw.raw_kv[off - dw.raw_start:], dw.raw_ik, T, off, 4, stream)
+        e[1].record(stream)
+        B.dsa_index_score_topk(dw.q_idx, dw.w, dw.state.pooled_ik, n, T, off, 4, k, tile,
+                               dw.scratch, dw.sel, dw.status, stream)
+        e[2].record(stream)
+        B.dsa_window_sparse_attn(dw.q, dw.raw_kv, dw.raw_start, dw.state.pooled_kv, n, dw.sel, k,
+                                 T, off, 4, wl.window, dw.scale, dw.out, dw.status, stream)
+        e[3].record(stream)
+        torch.cuda.synchronize()
+        if i >= 1:
+            comp["pool"].append(e[0].elapsed_time(e[1]))
+            comp["score_topk"].append(e[1].elapsed_time(e[2]))
+            comp["attention"].append(e[2].elapsed_time(e[3]))
+    comp_ms = {key: statistics.mean(v) for key, v in comp.items()}
+    dw.check_status()
+
+    # ---- end to end through the ABI with host buffers (pinned), copies timed
+    e2e = None
+    if not args.no_e2e:
+        host = {name: getattr(dw, name).cpu().pin_memory() for name in
+                ("raw_kv", "raw_ik", "q_idx", "w", "q")}
+        out_h = torch.empty(dw.out.shape, dtype=dw.out.dtype).pin_memory()
+        sel_h = torch.empty(dw.sel.shape, dtype=dw.sel.dtype).pin_memory()
+        h2d = sum(t.numel() * t.element_size() for t in host.values())
+        d2h = out_h.numel() * out_h.element_size() + sel_h.numel() * sel_h.element_size()
+
+        def e2e_step():
+            for name, t in host.items():
+                getattr(dw, name).copy_(t, non_blocking=True)
+            step()
+            out_h.copy_(dw.out, non_blocking=True)
+            sel_h.copy_(dw.sel, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        torch.cuda.synchronize()
+        ee = []
+        for i in range(max(3, args.steps // 2)):
+            flush.zero_()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            e2e_step()
+            b.record(stream)
+            torch.cuda.synchronize()
+            ee.append(a.elapsed_time(b))
+        ems = max_over_ranks(statistics.mean(ee), world, dev)
+        e2e = {"value": world * T / (ems * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": ems}
+
+    peaks, src = load_peaks()
+    t_st = comp_ms["score_topk"] * 1e-3
+    achieved = counts["score_flops"] / t_st / 1e12
+    attn_tf = counts["attn_flops"] / (comp_ms["attention"] * 1e-3) / 1e12
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": WORKLOAD_DESC, "name": wl.name, "chunk": T, "context": wl.end,
+                   "index_topk": wl.index_topk, "tile_rows": tile, "pooled_rows": n,
+                   "l2": "flushed between steps (512 MiB write, outside the step events)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "roofline": {"kernel": "indexer score + top-k (dsa_index_score_topk)", "bound": "tensor",
+                     "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": achieved / peaks["bf16_tflops"], "traffic": None,
+                     "peak_source": f"{src} bf16 dense (burst)",
+                     "algorithmic_flops_per_launch": counts["score_flops"]},
+        "components_ms": comp_ms,
+        "attention_roofline": {"achieved": attn_tf, "unit": "TFLOP/s",
+                               "frac": attn_tf / peaks["bf16_tflops"], "bound": "tensor"},
+        "gpu_launches": args.steps * (2 + 2 * math.ceil(T / tile)),
+        "clocks": clk.summary(),
+        "wall_s_timed_region": wall,
+    }
+    if e2e:
+        line["e2e"] = e2e
+    if rank == 0 and not args.no_cpu:
+        line["cpu_baseline"] = cpu_baseline(wl)
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,58 @@
+// Host-side internals shared by the translation units of libdsa.so: launch
+// entry points of each kernel family, tensor-map construction and argument checks.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "dsa.h"
+
+namespace dsa {
+
+constexpr int kRatio = DSA_RATIO;
+constexpr int kHI = DSA_INDEX_HEADS;
+constexpr int kDI = DSA_INDEX_DIM;
+constexpr int kH = DSA_HEADS;
+constexpr int kD = DSA_DIM;
+
+// Pooled rows per score block (MMA M), and the padded row stride of the score
+// scratch in floats.
+constexpr int kScoreBlock = 128;
+inline int64_t score_stride(int64_t n_pooled) {
+    return (n_pooled + kScoreBlock - 1) / kScoreBlock * kScoreBlock;
+}
+
+inline int64_t n_visible(int64_t t, int64_t n) {
+    int64_t v = (t + 1) / kRatio;
+    return v < n ? v : n;
+}
+
+inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// 2-D bf16 tensor map with 128-byte swizzle: `inner` elements per row (the
+// contiguous dimension), `rows` rows of `row_bytes` each, box of
+// box_inner x box_rows. Returns false if the driver rejects it.
+bool make_tmap_bf16(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
+                    uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows);
+
+int sm_count();
+
+// Launchers (stream-ordered, no host synchronization). Each returns DSA_OK or
+// DSA_ERR_CUDA; arguments are validated by the caller.
+int launch_pool_append(const dsa_pool_state &st, const void *raw_kv, const void *raw_ik,
+                       int64_t chunk, int64_t offset, cudaStream_t s);
+int launch_fill_selection(int32_t *sel, int64_t rows, int32_t k, int64_t offset, int64_t n,
+                          cudaStream_t s);
+int launch_score_tile(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const float *w,
+                      int64_t n, int64_t offset, int64_t r0, int64_t R, float *scores,
+                      int64_t stride, int32_t *status, cudaStream_t s);
+int launch_topk_tile(const float *scores, int64_t stride, int64_t n, int64_t offset, int64_t r0,
+                     int64_t R, int32_t k, int32_t *sel, int32_t *status, cudaStream_t s);
+int launch_attention(const void *q, const void *raw_kv, int64_t raw_start, int64_t raw_rows,
+                     const void *pooled_kv, int64_t n, const int32_t *sel, int32_t k,
+                     int64_t chunk, int64_t offset, int32_t window, float scale, void *out,
+                     int32_t *status, cudaStream_t s);
+
+}  // namespace dsa

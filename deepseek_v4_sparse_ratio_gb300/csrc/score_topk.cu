@@ -1,0 +1,582 @@
+// Steps (b) and (c): indexer scores with the pooled-ratio causal mask folded
+// into the epilogue, then per-row top-k, in bounded query-row tiles.
+//
+// "perf(deepseek_v4): faster exact DeepSeek-V4 prefill", Summary item 5 and
+// Performance: the DSA indexer scores every causally visible pooled row of
+// every query row (linear in context, FLOP-bound), and the pooled-ratio
+// causal mask is applied inside the score kernel's epilogue.
+// "perf(deepseek-v4): skip redundant all-pooled indexer scoring", Summary:
+// when every pooled row fits within index_topk the scoring and top-k are
+// skipped and the selection is the sequential indices.
+// "[Discussion] Tile indexed-attention scoring independently of the global
+// prefill chunk", Possible design: score/top-k run over bounded row tiles that
+// reuse one score scratch, so scratch is tile_rows x pooled rows.
+//
+// Score kernel (tcgen05): s[t,j] = sum_h w[t,h] * ReLU(q[t,h,:] . k[j,:]).
+// The contraction is a GEMM with the pooled keys on M (128 rows per MMA) and
+// (token, head) pairs on N (4 tokens x 64 heads = 256), K = 128. A persistent
+// CTA keeps the indexer queries of 8 tokens resident in shared memory (two
+// N=256 operands) and streams 128-row key blocks through a TMA ring; the
+// accumulators live in TMEM (2 x 256 columns, one per 4-token half), so the
+// epilogue thread that owns TMEM lane j holds every head of its tokens for
+// pooled row j and reduces them in registers: ReLU, multiply by w, sum over
+// heads in order h = 0..63, mask j >= n_vis(t) to -inf, store coalesced.
+//
+// Top-k kernel: one CTA per query row. Rows with n_vis <= k keep all visible
+// rows. Otherwise a 3-digit (11/11/10-bit) radix select over order-preserving
+// keys of the fp32 scores finds the k-th largest value and how many of its
+// equals to keep; a final pass in index order emits the kept indices
+// ascending, taking equal scores lowest index first.
+#include <math.h>
+
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace dsa {
+
+namespace {
+
+// ------------------------------------------------------------------ score kernel
+
+constexpr int kTok = 8;            // query rows per work unit
+constexpr int kStages = 2;         // key-block ring depth
+constexpr int kScoreThreads = 320; // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
+constexpr uint32_t kBBytes = 2 * 2 * 256 * 128;  // [half][k-chunk][256 rows][128 B]
+constexpr uint32_t kAStage = 2 * 128 * 128;      // [k-chunk][128 rows][128 B]
+constexpr uint32_t kOffB = 0;
+constexpr uint32_t kOffA = kOffB + kBBytes;
+constexpr uint32_t kOffW = kOffA + kStages * kAStage;
+constexpr uint32_t kOffBar = kOffW + kTok * kHI * 4;
+constexpr uint32_t kScoreSmem = kOffBar + 256 + 1024;  // + slack for 1024-B alignment
+
+struct ScoreParams {
+    const float *w;   // [chunk, 64]
+    float *scores;    // tile scratch [R, stride]
+    int64_t stride;   // floats per scratch row (multiple of 128)
+    int64_t n;        // pooled rows
+    int64_t offset;   // absolute position of chunk row 0
+    int64_t r0;       // first chunk row of the tile
+    int R;            // rows in the tile
+    int nseg;         // key-range segments per 8-row group
+    int NB;           // stride / 128
+    int n_units;      // ceil(R/8) * nseg
+    int32_t *status;
+};
+
+struct Unit {
+    int row0, nrow, b0, b1, kend;  // MMA over blocks [b0, kend), -inf fill over [kend, b1)
+};
+
+__device__ __forceinline__ Unit unit_geom(const ScoreParams &p, int u) {
+    Unit x;
+    const int g = u / p.nseg, s = u % p.nseg;
+    x.row0 = g * kTok;
+    x.nrow = min(kTok, p.R - x.row0);
+    const int64_t t_last = p.offset + p.r0 + x.row0 + x.nrow - 1;
+    const int64_t nv = min(p.n, (t_last + 1) / kRatio);
+    const int kb_vis = static_cast<int>((nv + kScoreBlock - 1) / kScoreBlock);
+    x.b0 = static_cast<int>(static_cast<int64_t>(s) * p.NB / p.nseg);
+    x.b1 = static_cast<int>(static_cast<int64_t>(s + 1) * p.NB / p.nseg);
+    x.kend = max(x.b0, min(x.b1, kb_vis));
+    return x;
+}
+
+// Wait that ignores the abort flag (used only to drain in-flight work).
+__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
+    const uint32_t b = smem_u32(bar);
+    const long long t0 = clock64();
+    while (!mbar_test(b, parity))
+        if (clock64() - t0 > kWaitBudget) break;
+}
+
+__device__ __forceinline__ void store_score(const ScoreParams &p, int row, int64_t j, float acc) {
+    if (row >= p.R) return;
+    const int64_t t = p.offset + p.r0 + row;
+    const int64_t nv = min(p.n, (t + 1) / kRatio);
+    // sum of (+0) and (-0) terms can be -0; keep one zero so key order is total
+    const float s = j < nv ? (acc == 0.0f ? 0.0f : acc) : -INFINITY;
+    __stcs(p.scores + static_cast<int64_t>(row) * p.stride + j, s);
+}
+
+__global__ void __launch_bounds__(kScoreThreads, 1)
+    score_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                 const ScoreParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *sB = smem + kOffB;
+    uint8_t *sA = smem + kOffA;
+    float *sW = reinterpret_cast<float *>(smem + kOffW);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
+    uint64_t *full = bars;                 // [kStages] key block landed
+    uint64_t *empty = bars + kStages;      // [kStages] key block consumed by the MMAs
+    uint64_t *b_full = bars + 2 * kStages; // queries landed
+    uint64_t *b_empty = b_full + 1;        // queries consumed
+    uint64_t *t_full = b_full + 2;         // [2] accumulator half ready
+    uint64_t *t_empty = b_full + 4;        // [2] accumulator half drained
+    uint64_t *drain = b_full + 6;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(b_full + 7);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        mbar_init(b_full, 1);
+        mbar_init(b_empty, 1);
+        for (int h = 0; h < 2; ++h) {
+            mbar_init(&t_full[h], 1);
+            mbar_init(&t_empty[h], 8);
+        }
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+    }
+    if (warp == 1) tmem_alloc(tmem_holder, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0 && lane == 0) {
+        // ---------------- TMA producer
+        const uint64_t pol_k = policy_evict_last();
+        const uint64_t pol_q = policy_evict_first();
+        int it = 0, bu = 0;
+        for (int u = blockIdx.x; u < p.n_units && !*abort_flag; u += gridDim.x) {
+            const Unit x = unit_geom(p, u);
+            if (x.kend <= x.b0) continue;
+            if (!mbar_wait(b_empty, (bu & 1) ^ 1, abort_flag, p.status)) break;
+            mbar_expect_tx(b_full, kBBytes);
+            const int qrow = static_cast<int>((p.r0 + x.row0) * kHI);
+            for (int half = 0; half < 2; ++half)
+                for (int kc = 0; kc < 2; ++kc)
+                    tma_load_2d(sB + (half * 2 + kc) * 32768, &tm_q, b_full, kc * 64,
+                                qrow + half * 256, pol_q);
+            ++bu;
+            bool ok = true;
+            for (int kb = x.b0; kb < x.kend; ++kb) {
+                const int s = it % kStages;
+                const uint32_t ph = (it / kStages) & 1;
+                if (!mbar_wait(&empty[s], ph ^ 1, abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                }
+                mbar_expect_tx(&full[s], kAStage);
+                for (int kc = 0; kc < 2; ++kc)
+                    tma_load_2d(sA + s * kAStage + kc * 16384, &tm_k, &full[s], kc * 64,
+                                kb * kScoreBlock, pol_k);
+                ++it;
+            }
+            if (!ok) break;
+        }
+        // make sure no copy into this CTA's shared memory is still in flight
+        for (int i = max(0, it - kStages); i < it; ++i)
+            drain_wait(&full[i % kStages], (i / kStages) & 1);
+        if (bu > 0) drain_wait(b_full, (bu - 1) & 1);
+    } else if (warp == 1 && lane == 0) {
+        // ---------------- MMA issuer
+        constexpr uint32_t idesc = idesc_bf16(128, 256, false, false);
+        int it = 0, bu = 0, tu0 = 0, tu1 = 0;
+        for (int u = blockIdx.x; u < p.n_units && !*abort_flag; u += gridDim.x) {
+            const Unit x = unit_geom(p, u);
+            if (x.kend <= x.b0) continue;
+            if (!mbar_wait(b_full, bu & 1, abort_flag, p.status)) break;
+            tc_fence_after();
+            ++bu;
+            bool ok = true;
+            for (int kb = x.b0; kb < x.kend && ok; ++kb) {
+                const int s = it % kStages;
+                if (!mbar_wait(&full[s], (it / kStages) & 1, abort_flag, p.status)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                for (int half = 0; half < 2; ++half) {
+                    int &tu = half ? tu1 : tu0;
+                    if (!mbar_wait(&t_empty[half], (tu & 1) ^ 1, abort_flag, p.status)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t d = tmem + half * 256;
+                    for (int kc = 0; kc < 2; ++kc) {
+                        const uint64_t ad =
+                            desc_sw128(smem_u32(sA + s * kAStage + kc * 16384), 16, 1024);
+                        const uint64_t bd =
+                            desc_sw128(smem_u32(sB + (half * 2 + kc) * 32768), 16, 1024);
+#pragma unroll
+                        for (int k4 = 0; k4 < 4; ++k4)
+                            mma_bf16(d, ad + 2 * k4, bd + 2 * k4, idesc, (kc | k4) != 0);
+                    }
+                    mma_commit(&t_full[half]);
+                    ++tu;
+                }
+                if (!ok) break;
+                mma_commit(&empty[s]);
+                ++it;
+            }
+            if (!ok) break;
+            mma_commit(b_empty);
+        }
+        // every MMA issued above must have finished before TMEM is released
+        mma_commit(drain);
+        drain_wait(drain, 0);
+    } else if (warp >= 2) {
+        // ---------------- epilogue: 8 warps; TMEM sub-partition = warp % 4
+        const int ew = warp - 2;
+        const int sp = warp & 3;
+        const int cg = ew >> 2;  // tokens {2cg, 2cg+1} of each 4-token half
+        const uint32_t lane_addr = tmem + (static_cast<uint32_t>(sp * 32) << 16);
+        int tu0 = 0, tu1 = 0;
+        // Every epilogue warp walks every unit so that the named barriers
+        // below always see all 256 threads, even after an abort.
+        for (int u = blockIdx.x; u < p.n_units; u += gridDim.x) {
+            const Unit x = unit_geom(p, u);
+            asm volatile("bar.sync 1, 256;" ::: "memory");
+            for (int i = ew * 32 + lane; i < kTok * kHI; i += 256) {
+                const int row = x.row0 + i / kHI;
+                sW[i] = row < p.R ? __ldg(&p.w[(p.r0 + row) * kHI + (i % kHI)]) : 0.0f;
+            }
+            asm volatile("bar.sync 1, 256;" ::: "memory");
+            bool ok = !*abort_flag;
+            for (int kb = x.b0; kb < x.b1 && ok; ++kb) {
+                const int64_t j = static_cast<int64_t>(kb) * kScoreBlock + sp * 32 + lane;
+                if (kb < x.kend) {
+                    for (int half = 0; half < 2; ++half) {
+                        int &tu = half ? tu1 : tu0;
+                        if (!mbar_wait(&t_full[half], tu & 1, abort_flag, p.status)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        ++tu;
+#pragma unroll 1
+                        for (int tt = 0; tt < 2; ++tt) {
+                            const int tl = cg * 2 + tt;
+                            const int ti = half * 4 + tl;
+                            uint32_t va[32], vb[32];
+                            const uint32_t col = half * 256 + tl * 64;
+                            tmem_ld32(lane_addr + col, va);
+                            tmem_ld32(lane_addr + col + 32, vb);
+                            tmem_wait_ld();
+                            const float4 *w4 = reinterpret_cast<const float4 *>(sW + ti * kHI);
+                            float acc = 0.0f;
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) {
+                                const float4 ww = w4[q];
+                                acc = fmaf(ww.x, fmaxf(__uint_as_float(va[4 * q + 0]), 0.0f), acc);
+                                acc = fmaf(ww.y, fmaxf(__uint_as_float(va[4 * q + 1]), 0.0f), acc);
+                                acc = fmaf(ww.z, fmaxf(__uint_as_float(va[4 * q + 2]), 0.0f), acc);
+                                acc = fmaf(ww.w, fmaxf(__uint_as_float(va[4 * q + 3]), 0.0f), acc);
+                            }
+#pragma unroll
+                            for (int q = 0; q < 8; ++q) {
+                                const float4 ww = w4[8 + q];
+                                acc = fmaf(ww.x, fmaxf(__uint_as_float(vb[4 * q + 0]), 0.0f), acc);
+                                acc = fmaf(ww.y, fmaxf(__uint_as_float(vb[4 * q + 1]), 0.0f), acc);
+                                acc = fmaf(ww.z, fmaxf(__uint_as_float(vb[4 * q + 2]), 0.0f), acc);
+                                acc = fmaf(ww.w, fmaxf(__uint_as_float(vb[4 * q + 3]), 0.0f), acc);
+                            }
+                            store_score(p, x.row0 + ti, j, acc);
+                        }
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0) mbar_arrive(&t_empty[half]);
+                    }
+                } else {
+                    for (int half = 0; half < 2; ++half)
+                        for (int tt = 0; tt < 2; ++tt)
+                            store_score(p, x.row0 + half * 4 + cg * 2 + tt, j, -INFINITY);
+                }
+            }
+        }
+    }
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
+}
+
+// ------------------------------------------------------------------ top-k kernel
+
+constexpr int kTopkThreads = 512;
+constexpr int kTopkWarps = kTopkThreads / 32;
+constexpr int kStageMaxFloats = 49152;  // rows up to this long are staged in shared memory
+
+__device__ __forceinline__ uint32_t order_key(float f) {
+    const uint32_t b = __float_as_uint(f);
+    return b ^ ((b & 0x80000000u) ? 0xFFFFFFFFu : 0x80000000u);
+}
+
+// Exclusive block-wide prefix sum of a per-thread value; *total gets the sum.
+__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *warp_sums,
+                                                    uint32_t *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    uint32_t inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+        if (lane >= o) inc += y;
+    }
+    if (lane == 31) warp_sums[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+        uint32_t x = lane < kTopkWarps ? warp_sums[lane] : 0;
+        uint32_t xi = x;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, xi, o);
+            if (lane >= o) xi += y;
+        }
+        if (lane < kTopkWarps) warp_sums[lane] = xi - x;
+        if (lane == kTopkWarps - 1) warp_sums[kTopkWarps] = xi;
+    }
+    __syncthreads();
+    const uint32_t r = warp_sums[warp] + inc - v;
+    *total = warp_sums[kTopkWarps];
+    __syncthreads();
+    return r;
+}
+
+template <bool kStaged>
+__global__ void __launch_bounds__(kTopkThreads)
+    topk_kernel(const float *__restrict__ scores, int64_t stride, int64_t n, int64_t offset,
+                int64_t r0, int32_t k, int32_t *__restrict__ sel) {
+    extern __shared__ float srow[];
+    __shared__ uint32_t hist[2048];
+    __shared__ uint32_t warp_sums[kTopkWarps + 1];
+    __shared__ uint32_t s_digit, s_above;
+
+    const int row = blockIdx.x;
+    const int64_t t = offset + r0 + row;
+    const int64_t L = min(n, (t + 1) / kRatio);
+    int32_t *out = sel + (r0 + row) * static_cast<int64_t>(k);
+    if (L <= k) {
+        for (int i = threadIdx.x; i < k; i += kTopkThreads) out[i] = i < L ? i : -1;
+        return;
+    }
+    const float *src = scores + static_cast<int64_t>(row) * stride;
+    if (kStaged) {
+        const float4 *s4 = reinterpret_cast<const float4 *>(src);
+        float4 *d4 = reinterpret_cast<float4 *>(srow);
+        for (int64_t i = threadIdx.x; i < L / 4; i += kTopkThreads) d4[i] = __ldcs(&s4[i]);
+        for (int64_t i = (L / 4) * 4 + threadIdx.x; i < L; i += kTopkThreads) srow[i] = src[i];
+        __syncthreads();
+        src = srow;
+    }
+
+    // ---- radix select of the k-th largest key: digits [31:21], [20:10], [9:0]
+    uint32_t prefix = 0;
+    uint32_t need = static_cast<uint32_t>(k);
+    for (int pass = 0; pass < 3; ++pass) {
+        const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+        const int bits = pass == 2 ? 10 : 11;
+        const int nb = 1 << bits;
+        for (int i = threadIdx.x; i < nb; i += kTopkThreads) hist[i] = 0;
+        __syncthreads();
+        for (int64_t j = threadIdx.x; j < L; j += kTopkThreads) {
+            const uint32_t u = order_key(src[j]);
+            if (pass == 0 || (u >> (shift + bits)) == prefix)
+                atomicAdd(&hist[(u >> shift) & (nb - 1)], 1u);
+        }
+        __syncthreads();
+        // thread i owns bins [hi-per*(i+1), hi-per*i): descending order over threads
+        const int per = nb / kTopkThreads;
+        const int top = nb - per * threadIdx.x;  // exclusive upper bin
+        uint32_t mine = 0;
+        for (int b = top - per; b < top; ++b) mine += hist[b];
+        uint32_t tot;
+        const uint32_t above_mine = block_excl_scan(mine, warp_sums, &tot);
+        uint32_t cum = above_mine;
+        for (int b = top - 1; b >= top - per; --b) {
+            const uint32_t c = hist[b];
+            if (cum < need && need <= cum + c) {
+                s_digit = static_cast<uint32_t>(b);
+                s_above = cum;
+            }
+            cum += c;
+        }
+        __syncthreads();
+        prefix = (prefix << bits) | s_digit;
+        need -= s_above;
+        __syncthreads();
+    }
+    const uint32_t thr = prefix;  // key of the k-th largest score
+    // `need` equal keys are kept, lowest indices first
+
+    // ---- emit kept indices in ascending order
+    uint32_t run_sel = 0, run_eq = 0;
+    for (int64_t base = 0; base < L; base += kTopkThreads) {
+        const int64_t j = base + threadIdx.x;
+        uint32_t gt = 0, eq = 0;
+        if (j < L) {
+            const uint32_t u = order_key(src[j]);
+            gt = u > thr;
+            eq = u == thr;
+        }
+        uint32_t tot;
+        const uint32_t ex = block_excl_scan((eq << 16) | gt, warp_sums, &tot);
+        const uint32_t gt_before = ex & 0xFFFFu, eq_before = ex >> 16;
+        const uint32_t eq_taken_before = min(run_eq + eq_before, need) - min(run_eq, need);
+        const bool take = gt || (eq && run_eq + eq_before < need);
+        if (take) out[run_sel + gt_before + eq_taken_before] = static_cast<int32_t>(j);
+        const uint32_t gt_tot = tot & 0xFFFFu, eq_tot = tot >> 16;
+        run_sel += gt_tot + (min(run_eq + eq_tot, need) - min(run_eq, need));
+        run_eq += eq_tot;
+    }
+}
+
+// Selection without scoring: sel[i, c] = c if c < n_vis(t) else -1 (n = 0: all -1).
+__global__ void fill_selection_kernel(int32_t *sel, int64_t rows, int32_t k, int64_t offset,
+                                      int64_t n) {
+    const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (idx >= rows * k) return;
+    const int64_t i = idx / k;
+    const int32_t c = static_cast<int32_t>(idx % k);
+    const int64_t nv = min(n, (offset + i + 1) / kRatio);
+    sel[idx] = c < nv ? c : -1;
+}
+
+int choose_segments(int groups, int NB, int sms) {
+    int best = 1;
+    double best_cost = 1e30;
+    for (int ns = 1; ns <= std::min(32, NB); ++ns) {
+        const int64_t units = static_cast<int64_t>(groups) * ns;
+        const int64_t waves = (units + sms - 1) / sms;
+        const double cost = static_cast<double>(waves) * (static_cast<double>(NB) / ns + 4.0);
+        if (cost < best_cost * 0.999) {
+            best_cost = cost;
+            best = ns;
+        }
+    }
+    return best;
+}
+
+}  // namespace
+
+int launch_fill_selection(int32_t *sel, int64_t rows, int32_t k, int64_t offset, int64_t n,
+                          cudaStream_t s) {
+    const int64_t total = rows * k;
+    fill_selection_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, s>>>(sel, rows, k,
+                                                                                   offset, n);
+    return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+int launch_score_tile(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const float *w, int64_t n,
+                      int64_t offset, int64_t r0, int64_t R, float *scores, int64_t stride,
+                      int32_t *status, cudaStream_t s) {
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kScoreSmem) != cudaSuccess)
+            return DSA_ERR_CUDA;
+        attr_set = true;
+    }
+    const int sms = std::max(1, sm_count());
+    ScoreParams p;
+    p.w = w;
+    p.scores = scores;
+    p.stride = stride;
+    p.n = n;
+    p.offset = offset;
+    p.r0 = r0;
+    p.R = static_cast<int>(R);
+    p.NB = static_cast<int>(stride / kScoreBlock);
+    const int groups = static_cast<int>((R + kTok - 1) / kTok);
+    p.nseg = choose_segments(groups, p.NB, sms);
+    p.n_units = groups * p.nseg;
+    p.status = status;
+    const int grid = std::min(p.n_units, sms);
+    score_kernel<<<grid, kScoreThreads, kScoreSmem, s>>>(tm_q, tm_k, p);
+    return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+int launch_topk_tile(const float *scores, int64_t stride, int64_t n, int64_t offset, int64_t r0,
+                     int64_t R, int32_t k, int32_t *sel, int32_t *status, cudaStream_t s) {
+    (void)status;
+    const int64_t Lmax = std::min<int64_t>(n, (offset + r0 + R) / kRatio);
+    if (Lmax <= kStageMaxFloats) {
+        const size_t bytes = static_cast<size_t>(std::max<int64_t>(Lmax, 4)) * sizeof(float);
+        static bool attr_set = false;
+        if (!attr_set) {
+            if (cudaFuncSetAttribute(topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     kStageMaxFloats * 4) != cudaSuccess)
+                return DSA_ERR_CUDA;
+            attr_set = true;
+        }
+        topk_kernel<true><<<static_cast<unsigned>(R), kTopkThreads, bytes, s>>>(scores, stride, n,
+                                                                               offset, r0, k, sel);
+    } else {
+        topk_kernel<false><<<static_cast<unsigned>(R), kTopkThreads, 0, s>>>(scores, stride, n,
+                                                                            offset, r0, k, sel);
+    }
+    return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+}
+
+// Checks shared by dsa_index_score_topk and dsa_prefill_chunk.
+int check_score_topk(const void *q_idx, const float *w, const void *pooled_ik, int64_t n,
+                     int64_t chunk, int64_t offset, int32_t ratio, int32_t k, int64_t tile_rows,
+                     const void *scratch, size_t scratch_bytes, const int32_t *sel) {
+    if (!sel || chunk <= 0 || offset < 0 || n < 0) return DSA_ERR_ARG;
+    if (ratio != kRatio || k <= 0 || tile_rows <= 0) return DSA_ERR_SHAPE;
+    if (n != (offset + chunk) / kRatio) return DSA_ERR_ARG;
+    if (!aligned16(sel)) return DSA_ERR_ARG;
+    if (n > k) {
+        if (!q_idx || !w || !pooled_ik || !aligned16(q_idx) || !aligned16(w) ||
+            !aligned16(pooled_ik))
+            return DSA_ERR_ARG;
+        const size_t need = dsa_score_scratch_bytes(std::min(tile_rows, chunk), n);
+        if (!scratch || !aligned16(scratch) || scratch_bytes < need) return DSA_ERR_SCRATCH;
+        if (chunk * kHI > (int64_t{1} << 31) - 1 || n > (int64_t{1} << 31) - 1)
+            return DSA_ERR_SHAPE;
+    }
+    return DSA_OK;
+}
+
+int run_score_topk(const void *q_idx, const float *w, const void *pooled_ik, int64_t n,
+                   int64_t chunk, int64_t offset, int32_t k, int64_t tile_rows, void *scratch,
+                   int32_t *sel, int32_t *status, cudaStream_t s) {
+    if (n == 0 || n <= k) return launch_fill_selection(sel, chunk, k, offset, n, s);
+    CUtensorMap tm_q, tm_k;
+    if (!make_tmap_bf16(&tm_q, q_idx, kDI, static_cast<uint64_t>(chunk) * kHI, kDI * 2, 64, 256))
+        return DSA_ERR_CUDA;
+    if (!make_tmap_bf16(&tm_k, pooled_ik, kDI, static_cast<uint64_t>(n), kDI * 2, 64, 128))
+        return DSA_ERR_CUDA;
+    const int64_t stride = score_stride(n);
+    float *scores = static_cast<float *>(scratch);
+    for (int64_t r0 = 0; r0 < chunk; r0 += tile_rows) {
+        const int64_t R = std::min(tile_rows, chunk - r0);
+        int rc = launch_score_tile(tm_q, tm_k, w, n, offset, r0, R, scores, stride, status, s);
+        if (rc != DSA_OK) return rc;
+        rc = launch_topk_tile(scores, stride, n, offset, r0, R, k, sel, status, s);
+        if (rc != DSA_OK) return rc;
+    }
+    return DSA_OK;
+}
+
+}  // namespace dsa
+
+extern "C" size_t dsa_score_scratch_bytes(int64_t tile_rows, int64_t n_pooled) {
+    if (tile_rows <= 0 || n_pooled <= 0) return 0;
+    return static_cast<size_t>(tile_rows) * static_cast<size_t>(dsa::score_stride(n_pooled)) *
+           sizeof(float);
+}
+
+extern "C" int dsa_index_score_topk(const void *q_idx, const float *w, const void *pooled_ik,
+                                    int64_t n_pooled, int64_t chunk, int64_t offset, int32_t ratio,
+                                    int32_t index_topk, int64_t tile_rows, void *scratch,
+                                    size_t scratch_bytes, int32_t *sel, int32_t *dev_status,
+                                    void *stream) {
+    using namespace dsa;
+    int rc = check_score_topk(q_idx, w, pooled_ik, n_pooled, chunk, offset, ratio, index_topk,
+                              tile_rows, scratch, scratch_bytes, sel);
+    if (rc != DSA_OK) return rc;
+    return run_score_topk(q_idx, w, pooled_ik, n_pooled, chunk, offset, index_topk, tile_rows,
+                          scratch, sel, dev_status, static_cast<cudaStream_t>(stream));
+}

@@ -33,9 +33,10 @@ _lib = None
 
 
 def build(force: bool = False) -> str:
-    """Compile dsa_oracle.c into liboracle.so with gcc (OpenMP, no FP contraction)."""
+    """Compile dsa_oracle.c into liboracle.so with gcc (OpenMP, no FP contraction,
+    no reassociation: -O3 only vectorises loops whose sums stay independent)."""
     if force or not os.path.exists(_LIB) or os.path.getmtime(_LIB) < os.path.getmtime(_SRC):
-        cmd = ["gcc", "-O2", "-fopenmp", "-ffp-contract=off", "-fPIC", "-shared",
+        cmd = ["gcc", "-O3", "-fopenmp", "-ffp-contract=off", "-fPIC", "-shared",
                "-o", _LIB + ".tmp", _SRC, "-lm"]
         subprocess.run(cmd, check=True)
         os.replace(_LIB + ".tmp", _LIB)

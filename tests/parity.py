@@ -1,0 +1,74 @@
+"""Comparison rules between the CUDA path and the oracle.
+
+Tolerances (stated by the workload definition of the path):
+  - pooled rows, remainder rows, counters: bit-exact;
+  - scores: |gpu - ref| <= 1e-3 * max(|ref|, A) where A = sum_h |w_h| ReLU(dot)
+    is the size of the summed terms (plain relative error is ill-conditioned
+    where positive and negative head terms cancel); masked entries exactly -inf;
+  - selection: bit-exact, except indices whose oracle score lies within
+    1e-3 relative (same scale as above) of the row's k-th score;
+  - attention: max|err| <= 1e-2 * max|ref| per (row, head) block... taken over
+    the whole compared set, as the workload states.
+"""
+import numpy as np
+
+SCORE_RTOL = 1e-3
+ATTN_RTOL = 1e-2
+
+
+def check_scores(gpu: np.ndarray, ref: np.ndarray, mag: np.ndarray):
+    fin = np.isfinite(ref)
+    assert np.array_equal(np.isneginf(gpu), ~fin), "mask differs"
+    err = np.abs(gpu[fin].astype(np.float64) - ref[fin].astype(np.float64))
+    bound = SCORE_RTOL * np.maximum(np.abs(ref[fin]).astype(np.float64), mag[fin])
+    bad = err > bound
+    assert not bad.any(), f"{bad.sum()} scores out of tolerance; worst {(err / bound).max():.3g}"
+    return float((err / np.maximum(bound, 1e-300)).max()) if err.size else 0.0
+
+
+def _kth(scores_row: np.ndarray, k: int):
+    idx = np.arange(scores_row.size)
+    order = np.lexsort((idx, -scores_row.astype(np.float64)))
+    return order[k - 1]
+
+
+def check_selection(gpu_sel: np.ndarray, ref_sel: np.ndarray, pos, n: int, k: int,
+                    ref_scores=None, ref_mag=None, ratio: int = 4):
+    """Compare selections row by row; ref_scores/ref_mag [R, n] for the band rule."""
+    pos = np.asarray(pos)
+    n_band = 0
+    for r, t in enumerate(pos):
+        nv = min((int(t) + 1) // ratio, n)
+        g, e = gpu_sel[r], ref_sel[r]
+        gv = g[g >= 0]
+        # structure: ascending, unique, in range, -1 padded at the end
+        assert np.all(np.diff(gv) > 0), f"row {r}: not strictly ascending"
+        assert gv.size == 0 or (gv[0] >= 0 and gv[-1] < nv), f"row {r}: index out of range"
+        assert np.all(g[gv.size:] == -1), f"row {r}: padding"
+        assert gv.size == min(nv, k), f"row {r}: {gv.size} kept, expected {min(nv, k)}"
+        if nv <= k or ref_scores is None:
+            assert np.array_equal(g, e), f"row {r}: selection differs"
+            continue
+        s = ref_scores[r, :nv].astype(np.float64)
+        a = ref_mag[r, :nv]
+        kk = _kth(ref_scores[r, :nv], k)
+        band = np.abs(s - s[kk]) <= SCORE_RTOL * max(abs(s[kk]), a[kk])
+        gs, es = np.zeros(nv, bool), np.zeros(nv, bool)
+        gs[gv] = True
+        es[e[e >= 0]] = True
+        diff = (gs != es) & ~band
+        assert not diff.any(), f"row {r}: {diff.sum()} indices differ outside the tie band"
+        n_band += int(((gs != es) & band).sum())
+    return n_band
+
+
+def bf16_to_f64(x) -> np.ndarray:
+    import torch
+    return x.float().cpu().numpy().astype(np.float64)
+
+
+def check_attention(gpu_out: np.ndarray, ref: np.ndarray):
+    err = np.abs(gpu_out - ref).max()
+    scale = np.abs(ref).max()
+    assert err <= ATTN_RTOL * scale, f"attention max|err| {err:.3g} > 1e-2 * {scale:.3g}"
+    return float(err / scale)

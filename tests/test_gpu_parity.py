@@ -1,0 +1,262 @@
+"""Parity of the CUDA path (through the C ABI) with the CPU oracle.
+
+Small cases compare every output; the five named workloads run at full size
+in the same launch configuration as the benchmark and compare sampled rows
+(evenly spaced, first and last row included) plus the whole pooled-cache
+state. Tolerances are in tests/parity.py.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from deepseek_v4_sparse_ratio_gb300 import _binding as B
+from deepseek_v4_sparse_ratio_gb300 import inputs
+from deepseek_v4_sparse_ratio_gb300.runner import DeviceWorkload
+
+from parity import bf16_to_f64, check_attention, check_scores, check_selection
+
+pytestmark = pytest.mark.gpu
+
+SCALE = 1.0 / math.sqrt(512)
+
+
+def _bits(t):
+    return oracle.as_bf16_bits(t.cpu())
+
+
+# --------------------------------------------------------------------------- (a) pooling
+
+@pytest.mark.parametrize("chunks", [[10], [5, 3, 1, 7, 16, 2, 300], [2046, 2052], [1, 1, 1, 1, 1]])
+def test_pool_append_bitexact(dsa, chunks):
+    wl = inputs.draw(inputs.small(11, chunks, index_topk=8))
+    st = B.PoolState(wl.end // 4 + 1)
+    ref = oracle.PoolState(4)
+    raw_kv, raw_ik = wl.t["raw_kv"].cuda(), wl.t["raw_ik"].cuda()
+    for _, s, T, off in wl.chunk_bounds():
+        B.dsa_pool_append(st, raw_kv[s:s + T], raw_ik[s:s + T], T, off)
+        ref.append(wl.t["raw_ik"][s:s + T], wl.t["raw_kv"][s:s + T], off)
+        assert (st.n_pooled, st.n_tokens, st.n_rem) == (ref.n_pooled, ref.n_tokens, ref.n_rem)
+        assert st.c.n_pooled_ik == st.c.n_pooled_kv
+    torch.cuda.synchronize()
+    n = ref.n_pooled
+    assert np.array_equal(_bits(st.pooled_kv[:n]), ref.pooled_kv)
+    assert np.array_equal(_bits(st.pooled_ik[:n]), ref.pooled_ik)
+    assert np.array_equal(_bits(st.rem_kv[:ref.n_rem]), ref.rem_kv)
+    assert np.array_equal(_bits(st.rem_ik[:ref.n_rem]), ref.rem_ik)
+
+
+def test_pool_ten_tokens_then_resume(dsa):
+    """The pages' example: 10 tokens -> 2 pooled rows + 2 remainder; then resume."""
+    wl = inputs.draw(inputs.small(3, [10, 6], index_topk=64))
+    st = B.PoolState(8)
+    raw_kv, raw_ik = wl.t["raw_kv"].cuda(), wl.t["raw_ik"].cuda()
+    B.dsa_pool_append(st, raw_kv[:10], raw_ik[:10], 10, 0)
+    assert (st.n_pooled, st.n_rem) == (2, 2)
+    B.dsa_pool_append(st, raw_kv[10:], raw_ik[10:], 6, 10)
+    assert (st.n_pooled, st.n_rem) == (4, 0)
+    ref = oracle.PoolState(4)
+    ref.append(wl.t["raw_ik"], wl.t["raw_kv"], 0)
+    assert np.array_equal(_bits(st.pooled_kv[:4]), ref.pooled_kv)
+    with pytest.raises(B.DsaError):
+        B.dsa_pool_append(st, raw_kv[:4], raw_ik[:4], 4, 12)   # wrong offset
+    assert st.n_tokens == 16
+
+
+# --------------------------------------------------------------------------- (b)(c) score/top-k
+
+def _score_case(seed, off, T, k, dup=False):
+    P = off // 4
+    g = torch.Generator().manual_seed(seed)
+    q_idx = torch.randn(T, 64, 128, generator=g).to(torch.bfloat16)
+    w = torch.randn(T, 64, generator=g) * 0.125
+    n = (off + T) // 4
+    pik = torch.randn(n, 128, generator=g).to(torch.bfloat16)
+    if dup:   # repeated key rows: exact score ties that top-k must break by index
+        pik[1::3] = pik[0:-1:3][: pik[1::3].shape[0]]
+    return q_idx, w, pik, n
+
+
+@pytest.mark.parametrize("off,T,k,tile", [(1000, 300, 64, 300), (0, 512, 64, 512),
+                                          (8188, 37, 100, 37), (4096, 1000, 512, 1000)])
+def test_scores_and_topk_match_oracle(dsa, off, T, k, tile):
+    q_idx, w, pik, n = _score_case(off + T, off, T, k)
+    sel = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    scratch = torch.empty(B.dsa_score_scratch_bytes(tile, n) // 4, dtype=torch.float32,
+                          device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.dsa_index_score_topk(q_idx.cuda(), w.cuda(), pik.cuda(), n, T, off, 4, k, tile, scratch,
+                           sel, status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    pos = off + np.arange(T)
+    ref_s, mag = oracle.index_scores(q_idx, w.numpy(), pos, pik, n)
+    stride = (n + 127) // 128 * 128
+    gpu_s = scratch[: T * stride].view(T, stride)[:, :n].cpu().numpy()
+    check_scores(gpu_s, ref_s, mag)
+    ref_sel = oracle.topk(ref_s, pos, n, 4, k)
+    check_selection(sel.cpu().numpy(), ref_sel, pos, n, k, ref_s, mag)
+
+
+def test_topk_ties_break_toward_lower_index(dsa):
+    off, T, k = 2000, 64, 40
+    q_idx, w, pik, n = _score_case(5, off, T, k, dup=True)
+    sel = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    scratch = torch.empty(B.dsa_score_scratch_bytes(T, n) // 4, dtype=torch.float32,
+                          device="cuda")
+    B.dsa_index_score_topk(q_idx.cuda(), w.cuda(), pik.cuda(), n, T, off, 4, k, T, scratch, sel)
+    torch.cuda.synchronize()
+    # the top-k decision is made on the GPU's own fp32 scores: replay it exactly
+    stride = (n + 127) // 128 * 128
+    gpu_s = scratch[: T * stride].view(T, stride)[:, :n].cpu().numpy()
+    pos = off + np.arange(T)
+    assert np.array_equal(sel.cpu().numpy(), oracle.topk(gpu_s, pos, n, 4, k))
+
+
+@pytest.mark.parametrize("tiles", [(1, 7, 64, 333), (512, 1000)])
+def test_tile_size_changes_no_index(dsa, tiles):
+    off, T, k = 4096, 1000, 256
+    q_idx, w, pik, n = _score_case(9, off, T, k)
+    args = [t.cuda() for t in (q_idx, w, pik)]
+    outs = []
+    for tile in tiles:
+        sel = torch.empty(T, k, dtype=torch.int32, device="cuda")
+        scratch = torch.empty(B.dsa_score_scratch_bytes(tile, n) // 4, dtype=torch.float32,
+                              device="cuda")
+        B.dsa_index_score_topk(*args, n, T, off, 4, k, tile, scratch, sel)
+        outs.append(sel.cpu())
+    for o in outs[1:]:
+        assert torch.equal(o, outs[0])
+
+
+@pytest.mark.parametrize("off,T,k", [(0, 10, 64), (0, 200, 50), (4000, 96, 1024)])
+def test_skip_path_equals_full_path(dsa, off, T, k):
+    """0 < n <= k: the skip path's selection equals the oracle's full path."""
+    q_idx, w, pik, n = _score_case(13, off, T, k)
+    assert 0 < n <= k
+    sel = torch.full((T, k), 7, dtype=torch.int32, device="cuda")
+    B.dsa_index_score_topk(None, None, None, n, T, off, 4, k, 16, None, sel)
+    pos = off + np.arange(T)
+    ref, s, _ = oracle.select(q_idx, w.numpy(), pos, pik, n, 4, k, force_full=True)
+    assert s is not None
+    assert np.array_equal(sel.cpu().numpy(), ref)
+
+
+def test_empty_pool_selects_nothing(dsa):
+    sel = torch.zeros(3, 8, dtype=torch.int32, device="cuda")
+    B.dsa_index_score_topk(None, None, None, 0, 3, 0, 4, 8, 3, None, sel)
+    assert torch.all(sel.cpu() == -1)
+
+
+# --------------------------------------------------------------------------- (d) attention
+
+def _attn_case(seed, off, T, n, k, window=128, full_sel=False):
+    g = torch.Generator().manual_seed(seed)
+    raw_start = max(0, off - window + 1) - 3
+    raw_start = max(raw_start, 0)
+    raw = torch.randn(off + T - raw_start, 512, generator=g).to(torch.bfloat16)
+    pooled = torch.randn(max(n, 1), 512, generator=g).to(torch.bfloat16)
+    q = torch.randn(T, 64, 512, generator=g).to(torch.bfloat16)
+    rng = np.random.default_rng(seed)
+    sel = np.full((T, k), -1, np.int32)
+    for i in range(T):
+        nv = min((off + i + 1) // 4, n)
+        m = min(nv, k)
+        pick = np.arange(m) if full_sel else np.sort(rng.choice(nv, size=m, replace=False))
+        sel[i, :m] = pick
+    return raw_start, raw, pooled, q, sel
+
+
+@pytest.mark.parametrize("off,T,k", [(0, 67, 16), (1000, 130, 64),
+                                     (5000, 40, 300), (0, 3, 4)])
+def test_attention_matches_oracle(dsa, off, T, k):
+    n = (off + T) // 4
+    raw_start, raw, pooled, q, sel = _attn_case(off + T + k, off, T, n, k)
+    out = torch.empty(T, 64, 512, dtype=torch.bfloat16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.dsa_window_sparse_attn(q.cuda(), raw.cuda(), raw_start, pooled.cuda(), n,
+                             torch.from_numpy(sel).cuda(), k, T, off, 4, 128, SCALE, out, status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    ref = oracle.attention(q, off + np.arange(T), raw, raw_start, pooled, n, sel, 128, SCALE)
+    check_attention(bf16_to_f64(out), ref)
+
+
+def test_attention_reports_bad_index_and_skips_it(dsa):
+    off, T, k = 400, 8, 16
+    n = (off + T) // 4
+    raw_start, raw, pooled, q, sel = _attn_case(3, off, T, n, k)
+    bad = sel.copy()
+    bad[2, -1] = n + 5          # beyond the pool: skipped, reported
+    good = sel.copy()
+    good[2, -1] = -1
+    outs = []
+    for s in (bad, good):
+        out = torch.empty(T, 64, 512, dtype=torch.bfloat16, device="cuda")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        B.dsa_window_sparse_attn(q.cuda(), raw.cuda(), raw_start, pooled.cuda(), n,
+                                 torch.from_numpy(s).cuda(), k, T, off, 4, 128, SCALE, out, status)
+        torch.cuda.synchronize()
+        outs.append((out.cpu(), status.item()))
+    assert outs[0][1] == B.DSA_ERR_BOUNDS and outs[1][1] == 0
+    assert torch.equal(outs[0][0], outs[1][0])
+
+
+# --------------------------------------------------------------------------- whole path
+
+def _oracle_prefix_state(wl):
+    if wl.off0:
+        return oracle.PoolState.from_prefix(wl.t["prefix_ik"], wl.t["prefix_kv"], wl.off0)
+    return oracle.PoolState(4)
+
+
+def run_workload_parity(wl, tile_rows, sample):
+    dw = DeviceWorkload(wl, tile_rows=tile_rows)
+    ref_state = _oracle_prefix_state(wl)
+    raw_all = torch.cat([wl.t["prefix_win"], wl.t["raw_kv"]], 0)
+    sels = []
+    for c, s, T, off in wl.chunk_bounds():
+        dw.run_chunk(c)
+        torch.cuda.synchronize()
+        dw.check_status()
+        rows = inputs.sample_rows(T, sample)
+        res = oracle.prefill_chunk(ref_state, wl.t["raw_ik"][s:s + T], wl.t["raw_kv"][s:s + T],
+                                   off, wl.t["q_idx"][s:s + T], wl.t["w"][s:s + T].numpy(),
+                                   wl.t["q"][s:s + T], raw_all, dw.raw_start, rows,
+                                   wl.index_topk, wl.window, SCALE)
+        assert dw.state.n_pooled == res["n"] == (off + T) // 4
+        gsel = dw.sel[:T].cpu().numpy()
+        sels.append(gsel)
+        check_selection(gsel[rows], res["sel"], res["pos"], res["n"], wl.index_topk,
+                        res["scores"], res["mag"])
+        check_attention(bf16_to_f64(dw.out[rows]), res["out"])
+    n = ref_state.n_pooled
+    lo = wl.prefix_pooled
+    assert np.array_equal(_bits(dw.state.pooled_kv[lo:n]), ref_state.pooled_kv[lo:n])
+    assert np.array_equal(_bits(dw.state.pooled_ik[lo:n]), ref_state.pooled_ik[lo:n])
+    assert dw.state.n_rem == ref_state.n_rem
+    return sels
+
+
+@pytest.mark.parametrize("name", ["zero_prefix_512", "two_chunks_4098", "prompt_16k"])
+def test_workload_parity(dsa, name):
+    wl = inputs.draw(inputs.workload(name))
+    sels = run_workload_parity(wl, wl.tile_rows[0], wl.sample_rows)
+    for tile in wl.tile_rows[1:]:
+        dw = DeviceWorkload(wl, tile_rows=tile)
+        for c, s, T, off in wl.chunk_bounds():
+            dw.run_chunk(c)
+            assert np.array_equal(dw.sel[:T].cpu().numpy(), sels[c]), f"tile {tile} chunk {c}"
+
+
+@pytest.mark.parametrize("name", ["ctx_128k", "ctx_1m"])
+def test_long_context_parity_and_tile_invariance(dsa, name):
+    wl = inputs.draw(inputs.workload(name))
+    sels = run_workload_parity(wl, wl.tile_rows[0], wl.sample_rows)
+    other = wl.tile_rows[1]
+    dw = DeviceWorkload(wl, tile_rows=other)
+    dw.run_chunk(0)
+    torch.cuda.synchronize()
+    assert np.array_equal(dw.sel[:wl.chunks[0]].cpu().numpy(), sels[0]), "tiling changed an index"
