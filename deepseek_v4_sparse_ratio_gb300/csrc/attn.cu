@@ -9,13 +9,25 @@
 // prefill chunk", Possible design step 4: the selected rows feed the indexed
 // attention.
 //
-// Keys of (t, h): raw rows u = max(0, t-W+1) .. t, then pooled rows sel[t, :]
-// that are >= 0. One 512-wide row is both key and value for all 64 heads.
-// Softmax runs online in fp32 (exp2 of log2e-scaled logits); the output is
-// normalised once at the end and stored as bf16.
+// Keys of (t, h): raw rows u = max(0, t-W+1) .. t, then the first
+// min(k, n_vis(t)) entries of sel[t, :] (entries that are -1 or outside
+// [0, n_vis(t)) are skipped; the latter are reported). One 512-wide row is both
+// key and value for all 64 heads.
 //
-// This version is one warp per (token, head): lane l owns dims 16l..16l+15 of
-// q, of every key row it reads, and of the output accumulator.
+// tcgen05 design, one token at a time per CTA (persistent over tokens), keys
+// in blocks of 128 rows (window rows by a TMA tile load, selected rows by TMA
+// gather4), everything transposed so the 128 keys sit on the MMA's M:
+//   S^T[key, head]  = K_blk[128 x 512] . Q_t^T      (M=128, N=64, K=512)
+//   O^T[d, head]   += V_blk^T[512 x 128] . P^T       (4 x (M=128, N=64, K=128))
+// K_blk and V_blk are the same shared-memory tile (K = V): 8 chunks of
+// [128 rows x 64 dims] with 128-byte swizzle, read K-major by the first MMA and
+// MN-major by the second. S^T (64 columns) and O^T (4 x 64 columns) live in
+// TMEM. Four softmax warps own TMEM lanes = keys: they mask, run the online
+// softmax in the log2 domain (exp2 of scale*log2e*logit - running max) and
+// write P^T as bf16. The running max is only raised when some logit exceeds it
+// by more than 8 (log2 units): P then stays <= 256, and the rescale of O^T
+// and of the partial sums is skipped on most blocks without changing the
+// result (the same max divides out at the end). Output = O^T / sum, bf16.
 #include <math.h>
 
 #include "common.cuh"
@@ -24,86 +36,432 @@ namespace dsa {
 
 namespace {
 
-constexpr int kAttnWarps = 8;  // heads per CTA
-
-__device__ __forceinline__ void load16(const __nv_bfloat16 *p, float (&x)[16]) {
-    const uint4 *v = reinterpret_cast<const uint4 *>(p);
-    const uint4 a = __ldg(v), b = __ldg(v + 1);
-    x[0] = bf16lo(a.x); x[1] = bf16hi(a.x); x[2] = bf16lo(a.y); x[3] = bf16hi(a.y);
-    x[4] = bf16lo(a.z); x[5] = bf16hi(a.z); x[6] = bf16lo(a.w); x[7] = bf16hi(a.w);
-    x[8] = bf16lo(b.x); x[9] = bf16hi(b.x); x[10] = bf16lo(b.y); x[11] = bf16hi(b.y);
-    x[12] = bf16lo(b.z); x[13] = bf16hi(b.z); x[14] = bf16lo(b.w); x[15] = bf16hi(b.w);
-}
+constexpr int kAttnThreads = 192;  // warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 softmax
+constexpr uint32_t kOffQ = 0;                 // 8 chunks x [64 heads x 128 B]
+constexpr uint32_t kOffKV = 65536;            // 8 chunks x [128 keys x 128 B]
+constexpr uint32_t kOffP = 65536 + 131072;    // [128 keys x 64 heads] bf16, MN-major
+constexpr uint32_t kOffRed = kOffP + 16384;   // [4 warps][64] fp32 block maxima
+constexpr uint32_t kOffL = kOffRed + 1024;    // [4 warps][64] fp32 partial sums
+constexpr uint32_t kOffLinv = kOffL + 1024;   // [64] 1/sum
+constexpr uint32_t kOffM = kOffLinv + 256;    // [2][64] running max (double-buffered)
+constexpr uint32_t kOffAlpha = kOffM + 512;   // [64] rescale factors
+constexpr uint32_t kOffBar = kOffAlpha + 256;
+constexpr uint32_t kAttnSmem = kOffBar + 256 + 1024;
+constexpr uint32_t kSCol = 0;    // S^T: 64 TMEM columns
+constexpr uint32_t kOCol = 256;  // O^T: 4 d-tiles x 64 columns
+constexpr float kRescale = 8.0f;
 
 struct AttnParams {
-    const __nv_bfloat16 *q;
-    const __nv_bfloat16 *raw_kv;
-    int64_t raw_start;
-    const __nv_bfloat16 *pooled_kv;
-    int64_t n;
     const int32_t *sel;
     int32_t k;
+    int64_t n;
     int64_t offset;
+    int64_t raw_start;
     int32_t window;
-    float scale_log2;  // softmax scale * log2(e)
+    float c;  // softmax scale * log2(e)
     __nv_bfloat16 *out;
+    int T;
     int32_t *status;
 };
 
-__device__ __forceinline__ void attend_row(const __nv_bfloat16 *row, int lane, const float (&qv)[16],
-                                           float scale_log2, float &m, float &l, float (&o)[16]) {
-    float kv[16];
-    load16(row + lane * 16, kv);
-    float s = 0.0f;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) s = fmaf(qv[i], kv[i], s);
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) s += __shfl_xor_sync(0xFFFFFFFFu, s, off);
-    s *= scale_log2;
-    const float m_new = fmaxf(m, s);
-    const float corr = exp2f(m - m_new);
-    const float pr = exp2f(s - m_new);
-    l = l * corr + pr;
-#pragma unroll
-    for (int i = 0; i < 16; ++i) o[i] = fmaf(pr, kv[i], o[i] * corr);
-    m = m_new;
+struct TokenInfo {
+    int64_t t, nv, u0;
+    int nwb, nsel, nb;
+};
+
+__device__ __forceinline__ TokenInfo token_info(const AttnParams &p, int i) {
+    TokenInfo x;
+    x.t = p.offset + i;
+    x.nv = min(p.n, (x.t + 1) / kRatio);
+    x.u0 = max(int64_t{0}, x.t - p.window + 1);
+    const int64_t nwin = x.t - x.u0 + 1;
+    x.nwb = static_cast<int>((nwin + 127) / 128);
+    x.nsel = static_cast<int>(min(static_cast<int64_t>(p.k), x.nv));
+    x.nb = x.nwb + (x.nsel + 127) / 128;
+    return x;
 }
 
-__global__ void __launch_bounds__(kAttnWarps * 32) attn_warp_kernel(const AttnParams p) {
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int64_t i = blockIdx.x / (kH / kAttnWarps);
-    const int h = (blockIdx.x % (kH / kAttnWarps)) * kAttnWarps + warp;
-    const int64_t t = p.offset + i;
-    float qv[16];
-    load16(p.q + (i * kH + h) * kD + lane * 16, qv);
-    float m = -INFINITY, l = 0.0f, o[16];
-#pragma unroll
-    for (int e = 0; e < 16; ++e) o[e] = 0.0f;
+__device__ __forceinline__ float redux_max(float v) {
+    float r;
+    asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(v));
+    return r;
+}
 
-    const int64_t u0 = t - p.window + 1 > 0 ? t - p.window + 1 : 0;
-    for (int64_t u = u0; u <= t; ++u)
-        attend_row(p.raw_kv + (u - p.raw_start) * kD, lane, qv, p.scale_log2, m, l, o);
-    const int64_t nv = min(p.n, (t + 1) / kRatio);
-    const int32_t *srow = p.sel + i * p.k;
-    for (int c = 0; c < p.k; ++c) {
-        const int32_t j = __ldg(&srow[c]);
-        if (j < 0) continue;
-        if (j >= nv) {
-            if (lane == 0 && h == 0) report(p.status, DSA_ERR_BOUNDS);
-            continue;
-        }
-        attend_row(p.pooled_kv + static_cast<int64_t>(j) * kD, lane, qv, p.scale_log2, m, l, o);
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// OR of `pred` over the 128 softmax threads (named barrier 1).
+__device__ __forceinline__ bool vote_any_128(bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.b32 p, %1, 0;\n bar.red.or.pred q, 1, 128, p;\n"
+        " selp.b32 %0, 1, 0, q;\n}\n"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred))
+        : "memory");
+    return r != 0;
+}
+
+__device__ __forceinline__ void bar_softmax() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
+    const uint32_t b = smem_u32(bar);
+    const long long t0 = clock64();
+    while (!mbar_test(b, parity))
+        if (clock64() - t0 > kWaitBudget) break;
+}
+
+__global__ void __launch_bounds__(kAttnThreads, 1)
+    attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_raw,
+                const __grid_constant__ CUtensorMap tm_pool, const AttnParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *sQ = smem + kOffQ;
+    uint8_t *sKV = smem + kOffKV;
+    uint8_t *sP = smem + kOffP;
+    float *sRed = reinterpret_cast<float *>(smem + kOffRed);
+    float *sL = reinterpret_cast<float *>(smem + kOffL);
+    float *sLinv = reinterpret_cast<float *>(smem + kOffLinv);
+    float *sM = reinterpret_cast<float *>(smem + kOffM);
+    float *sAlpha = reinterpret_cast<float *>(smem + kOffAlpha);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
+    uint64_t *q_full = bars + 0;
+    uint64_t *q_free = bars + 1;
+    uint64_t *kv_full = bars + 2;   // [8] chunk landed
+    uint64_t *kv_free = bars + 10;  // [4] chunk pair (d-tile) consumed by PV
+    uint64_t *s_full = bars + 14;
+    uint64_t *p_full = bars + 15;
+    uint64_t *o_full = bars + 16;
+    uint64_t *o_free = bars + 17;
+    uint64_t *drain = bars + 18;
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 19);
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (threadIdx.x == 0) {
+        mbar_init(q_full, 1);
+        mbar_init(q_free, 1);
+        for (int c = 0; c < 8; ++c) mbar_init(&kv_full[c], 1);
+        for (int m = 0; m < 4; ++m) mbar_init(&kv_free[m], 1);
+        mbar_init(s_full, 1);
+        mbar_init(p_full, 128);
+        mbar_init(o_full, 1);
+        mbar_init(o_free, 4);
+        mbar_init(drain, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
     }
-    const float inv = 1.0f / l;
-    uint32_t packed[8];
+    if (warp == 1) tmem_alloc(tmem_holder, 512);
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0) {
+        // ---------------- TMA producer (lane 0 waits and loads tiles; all lanes gather)
+        const uint64_t pol_stream = policy_evict_first();
+        const uint64_t pol_keep = policy_evict_last();
+        int tok = 0, g = 0, last_q = -1;
+        bool ok = true;
+        for (int i = blockIdx.x; i < p.T && ok; i += gridDim.x, ++tok) {
+            const TokenInfo x = token_info(p, i);
+            if (lane == 0) {
+                ok = mbar_wait(q_free, (tok & 1) ^ 1, abort_flag, p.status);
+                if (ok) {
+                    mbar_expect_tx(q_full, 65536);
+                    for (int c = 0; c < 8; ++c)
+                        tma_load_2d(sQ + c * 8192, &tm_q, q_full, c * 64, i * 64, pol_stream);
+                    last_q = tok;
+                }
+            }
+            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+            for (int b = 0; b < x.nb && ok; ++b, ++g) {
+                const bool win = b < x.nwb;
+                int y[4] = {0, 0, 0, 0};
+                if (!win) {
+                    const int base = (b - x.nwb) * 128 + lane * 4;
+                    const int32_t *srow = p.sel + static_cast<int64_t>(i) * p.k;
 #pragma unroll
-    for (int e = 0; e < 8; ++e) {
-        const __nv_bfloat162 v = __floats2bfloat162_rn(o[2 * e] * inv, o[2 * e + 1] * inv);
-        packed[e] = *reinterpret_cast<const uint32_t *>(&v);
+                    for (int e = 0; e < 4; ++e) {
+                        const int pos = base + e;
+                        const int32_t j = pos < x.nsel ? __ldg(&srow[pos]) : -1;
+                        const bool valid = j >= 0 && j < x.nv;
+                        if (!valid && j != -1) report(p.status, DSA_ERR_BOUNDS);
+                        y[e] = valid ? j : 0;
+                    }
+                }
+                for (int m = 0; m < 4 && ok; ++m) {
+                    if (lane == 0) {
+                        ok = mbar_wait(&kv_free[m], (g & 1) ^ 1, abort_flag, p.status);
+                        if (ok) {
+                            mbar_expect_tx(&kv_full[2 * m], 16384);
+                            mbar_expect_tx(&kv_full[2 * m + 1], 16384);
+                            if (win) {
+                                const int row = static_cast<int>(x.u0 + 128 * b - p.raw_start);
+                                for (int c = 2 * m; c < 2 * m + 2; ++c)
+                                    tma_load_2d(sKV + c * 16384, &tm_raw, &kv_full[c], c * 64, row,
+                                                pol_keep);
+                            }
+                        }
+                    }
+                    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+                    if (ok && !win) {
+                        for (int c = 2 * m; c < 2 * m + 2; ++c)
+                            tma_gather4(sKV + c * 16384 + lane * 512, &tm_pool, &kv_full[c],
+                                        c * 64, y[0], y[1], y[2], y[3], pol_keep);
+                    }
+                }
+            }
+        }
+        // no copy into this CTA's shared memory may still be in flight at exit
+        if (lane == 0) {
+            if (g > 0)
+                for (int c = 0; c < 8; ++c) drain_wait(&kv_full[c], (g - 1) & 1);
+            if (last_q >= 0) drain_wait(q_full, last_q & 1);
+        }
+    } else if (warp == 1) {
+        // ---------------- MMA issuer
+        if (lane == 0) {
+            constexpr uint32_t idesc_qk = idesc_bf16(128, 64, false, false);
+            constexpr uint32_t idesc_pv = idesc_bf16(128, 64, true, true);
+            int tok = 0, g = 0;
+            bool ok = true;
+            for (int i = blockIdx.x; i < p.T && ok; i += gridDim.x, ++tok) {
+                const TokenInfo x = token_info(p, i);
+                if (!(ok = mbar_wait(q_full, tok & 1, abort_flag, p.status))) break;
+                tc_fence_after();
+                for (int b = 0; b < x.nb && ok; ++b, ++g) {
+                    for (int c = 0; c < 8; ++c) {
+                        if (!(ok = mbar_wait(&kv_full[c], g & 1, abort_flag, p.status))) break;
+                        tc_fence_after();
+                        const uint64_t ad = desc_sw128(smem_u32(sKV + c * 16384), 16, 1024);
+                        const uint64_t bd = desc_sw128(smem_u32(sQ + c * 8192), 16, 1024);
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_bf16(tmem + kSCol, ad + 2 * kk, bd + 2 * kk, idesc_qk,
+                                     (c | kk) != 0);
+                    }
+                    if (!ok) break;
+                    mma_commit(s_full);
+                    if (b == x.nb - 1) mma_commit(q_free);
+                    if (!(ok = mbar_wait(p_full, g & 1, abort_flag, p.status))) break;
+                    tc_fence_after();
+                    if (b == 0 && tok > 0) {
+                        if (!(ok = mbar_wait(o_free, (tok - 1) & 1, abort_flag, p.status))) break;
+                        tc_fence_after();
+                    }
+                    for (int m = 0; m < 4; ++m) {
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk) {
+                            const uint64_t ad = desc_sw128(
+                                smem_u32(sKV + 2 * m * 16384 + kk * 2048), 16384, 1024);
+                            const uint64_t bd = desc_sw128(smem_u32(sP + kk * 2048), 8192, 1024);
+                            mma_bf16(tmem + kOCol + 64 * m, ad, bd, idesc_pv, (b > 0 || kk > 0));
+                        }
+                        mma_commit(&kv_free[m]);
+                    }
+                    if (b == x.nb - 1) mma_commit(o_full);
+                }
+            }
+            mma_commit(drain);
+            drain_wait(drain, 0);
+        }
+    } else {
+        // ---------------- softmax + epilogue: thread owns TMEM lane kl (a key, later a dim)
+        const int sp = warp & 3;
+        const int kl = sp * 32 + lane;
+        const uint32_t lane_base = tmem + (static_cast<uint32_t>(sp * 32) << 16);
+        int tok = 0, g = 0, cur = 0;
+        for (int i = blockIdx.x; i < p.T; i += gridDim.x, ++tok) {
+            const TokenInfo x = token_info(p, i);
+            float l[64];
+#pragma unroll
+            for (int h = 0; h < 64; ++h) l[h] = 0.0f;
+            if (kl < 64) sM[cur * 64 + kl] = -INFINITY;
+            bar_softmax();
+            for (int b = 0; b < x.nb; ++b, ++g) {
+                const bool live = mbar_wait(s_full, g & 1, abort_flag, p.status);
+                tc_fence_after();
+                uint32_t sa[32], sb[32];
+                if (live) {
+                    tmem_ld32(lane_base + kSCol, sa);
+                    tmem_ld32(lane_base + kSCol + 32, sb);
+                    tmem_wait_ld();
+                }
+                bool valid;
+                if (b < x.nwb) {
+                    valid = x.u0 + 128 * b + kl <= x.t;
+                } else {
+                    const int pos = (b - x.nwb) * 128 + kl;
+                    const int32_t j =
+                        pos < x.nsel ? __ldg(&p.sel[static_cast<int64_t>(i) * p.k + pos]) : -1;
+                    valid = j >= 0 && j < x.nv;
+                }
+                valid = valid && live;
+                const float *m_now = sM + cur * 64;
+                bool exceed = false;
+#pragma unroll
+                for (int h = 0; h < 64; h += 4) {
+                    const float4 m4 = *reinterpret_cast<const float4 *>(&m_now[h]);
+                    const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+#pragma unroll
+                    for (int e = 0; e < 4; ++e) {
+                        const float s = __uint_as_float(h + e < 32 ? sa[h + e] : sb[h + e - 32]);
+                        exceed |= valid && fmaf(s, p.c, -mm[e]) > kRescale;
+                    }
+                }
+                if (vote_any_128(exceed)) {
+                    // exact block maxima -> new running max, then rescale sums and O^T
+#pragma unroll
+                    for (int h = 0; h < 64; ++h) {
+                        const float s = __uint_as_float(h < 32 ? sa[h] : sb[h - 32]);
+                        const float wm = redux_max(valid ? s * p.c : -INFINITY);
+                        if (lane == (h & 31)) sRed[sp * 64 + h] = wm;
+                    }
+                    bar_softmax();
+                    if (kl < 64) {
+                        const float bm = fmaxf(fmaxf(sRed[kl], sRed[64 + kl]),
+                                               fmaxf(sRed[128 + kl], sRed[192 + kl]));
+                        const float m_old = sM[cur * 64 + kl];
+                        const float m_new = fmaxf(m_old, bm);
+                        sM[(cur ^ 1) * 64 + kl] = m_new;
+                        sAlpha[kl] = ex2(m_old - m_new);
+                    }
+                    bar_softmax();
+                    cur ^= 1;
+#pragma unroll
+                    for (int h = 0; h < 64; h += 4) {
+                        const float4 a4 = *reinterpret_cast<const float4 *>(&sAlpha[h]);
+                        l[h] *= a4.x;
+                        l[h + 1] *= a4.y;
+                        l[h + 2] *= a4.z;
+                        l[h + 3] *= a4.w;
+                    }
+                    if (b > 0 && live) {
+#pragma unroll 1
+                        for (int c32 = 0; c32 < 8; ++c32) {
+                            uint32_t oa[32];
+                            const uint32_t col = lane_base + kOCol + 32 * c32;
+                            const float *al = sAlpha + (c32 & 1) * 32;
+                            tmem_ld32(col, oa);
+                            tmem_wait_ld();
+#pragma unroll
+                            for (int h = 0; h < 32; ++h)
+                                oa[h] = __float_as_uint(__uint_as_float(oa[h]) * al[h]);
+                            tmem_st32(col, oa);
+                        }
+                        tmem_wait_st();
+                    }
+                }
+                // P^T row for this key: 64 heads, bf16, 128-byte swizzled row
+                const float *m_use = sM + cur * 64;
+                uint8_t *prow = sP + kl * 128;
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    uint32_t pk[4];
+#pragma unroll
+                    for (int h2 = 0; h2 < 8; h2 += 4) {
+                        const int h = 8 * q + h2;
+                        const float4 m4 = *reinterpret_cast<const float4 *>(&m_use[h]);
+                        const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+                        float pr[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float sv =
+                                __uint_as_float(h + e < 32 ? sa[h + e] : sb[h + e - 32]);
+                            pr[e] = valid ? ex2(fmaf(sv, p.c, -mm[e])) : 0.0f;
+                            l[h + e] += pr[e];
+                        }
+                        const __nv_bfloat162 v0 = __floats2bfloat162_rn(pr[0], pr[1]);
+                        const __nv_bfloat162 v1 = __floats2bfloat162_rn(pr[2], pr[3]);
+                        pk[h2 / 2] = *reinterpret_cast<const uint32_t *>(&v0);
+                        pk[h2 / 2 + 1] = *reinterpret_cast<const uint32_t *>(&v1);
+                    }
+                    *reinterpret_cast<uint4 *>(prow + ((q ^ (kl & 7)) << 4)) =
+                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
+                }
+                fence_proxy_async_smem();
+                tc_fence_before();
+                mbar_arrive(p_full);
+            }
+            // ---- token end: sums over keys, then O^T / sum -> out[t, h, d]
+            const bool live = mbar_wait(o_full, tok & 1, abort_flag, p.status);
+            tc_fence_after();
+            // transpose-reduce the 64 partial sums across the warp: lane ends
+            // with the warp's totals for heads 2*lane and 2*lane+1
+            {
+                float *v = l;
+#pragma unroll
+                for (int i2 = 0; i2 < 32; ++i2) {
+                    const bool hi = lane & 16;
+                    const float send = hi ? v[i2] : v[i2 + 32];
+                    const float keep = hi ? v[i2 + 32] : v[i2];
+                    v[i2] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 16);
+                }
+#pragma unroll
+                for (int i2 = 0; i2 < 16; ++i2) {
+                    const bool hi = lane & 8;
+                    const float send = hi ? v[i2] : v[i2 + 16];
+                    const float keep = hi ? v[i2 + 16] : v[i2];
+                    v[i2] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 8);
+                }
+#pragma unroll
+                for (int i2 = 0; i2 < 8; ++i2) {
+                    const bool hi = lane & 4;
+                    const float send = hi ? v[i2] : v[i2 + 8];
+                    const float keep = hi ? v[i2 + 8] : v[i2];
+                    v[i2] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 4);
+                }
+#pragma unroll
+                for (int i2 = 0; i2 < 4; ++i2) {
+                    const bool hi = lane & 2;
+                    const float send = hi ? v[i2] : v[i2 + 4];
+                    const float keep = hi ? v[i2 + 4] : v[i2];
+                    v[i2] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 2);
+                }
+#pragma unroll
+                for (int i2 = 0; i2 < 2; ++i2) {
+                    const bool hi = lane & 1;
+                    const float send = hi ? v[i2] : v[i2 + 2];
+                    const float keep = hi ? v[i2 + 2] : v[i2];
+                    v[i2] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 1);
+                }
+                *reinterpret_cast<float2 *>(&sL[sp * 64 + 2 * lane]) = make_float2(v[0], v[1]);
+            }
+            bar_softmax();
+            if (kl < 64)
+                sLinv[kl] = 1.0f / (sL[kl] + sL[64 + kl] + sL[128 + kl] + sL[192 + kl]);
+            bar_softmax();
+            if (live) {
+                __nv_bfloat16 *orow = p.out + static_cast<int64_t>(i) * (kH * kD);
+#pragma unroll 1
+                for (int c32 = 0; c32 < 8; ++c32) {
+                    uint32_t oa[32];
+                    tmem_ld32(lane_base + kOCol + 32 * c32, oa);
+                    tmem_wait_ld();
+                    const int d = 128 * (c32 >> 1) + kl;
+                    const int h0 = (c32 & 1) * 32;
+#pragma unroll
+                    for (int h = 0; h < 32; ++h)
+                        orow[(h0 + h) * kD + d] =
+                            __float2bfloat16_rn(__uint_as_float(oa[h]) * sLinv[h0 + h]);
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(o_free);
+        }
     }
-    uint4 *dst = reinterpret_cast<uint4 *>(p.out + (i * kH + h) * kD + lane * 16);
-    dst[0] = make_uint4(packed[0], packed[1], packed[2], packed[3]);
-    dst[1] = make_uint4(packed[4], packed[5], packed[6], packed[7]);
+    __syncthreads();
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, 512);
+    }
 }
 
 }  // namespace
@@ -112,22 +470,35 @@ int launch_attention(const void *q, const void *raw_kv, int64_t raw_start, int64
                      const void *pooled_kv, int64_t n, const int32_t *sel, int32_t k,
                      int64_t chunk, int64_t offset, int32_t window, float scale, void *out,
                      int32_t *status, cudaStream_t s) {
-    (void)raw_rows;
+    static bool attr_set = false;
+    if (!attr_set) {
+        if (cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kAttnSmem) != cudaSuccess)
+            return DSA_ERR_CUDA;
+        attr_set = true;
+    }
+    CUtensorMap tm_q, tm_raw, tm_pool;
+    if (!make_tmap_bf16(&tm_q, q, kD, static_cast<uint64_t>(chunk) * kH, kD * 2, 64, 64))
+        return DSA_ERR_CUDA;
+    if (!make_tmap_bf16(&tm_raw, raw_kv, kD, static_cast<uint64_t>(raw_rows), kD * 2, 64, 128))
+        return DSA_ERR_CUDA;
+    // with no pooled rows the gather map is never used; point it at raw_kv
+    const void *pool_base = n > 0 ? pooled_kv : raw_kv;
+    const uint64_t pool_rows = n > 0 ? static_cast<uint64_t>(n) : static_cast<uint64_t>(raw_rows);
+    if (!make_tmap_bf16(&tm_pool, pool_base, kD, pool_rows, kD * 2, 64, 1)) return DSA_ERR_CUDA;
     AttnParams p;
-    p.q = static_cast<const __nv_bfloat16 *>(q);
-    p.raw_kv = static_cast<const __nv_bfloat16 *>(raw_kv);
-    p.raw_start = raw_start;
-    p.pooled_kv = static_cast<const __nv_bfloat16 *>(pooled_kv);
-    p.n = n;
     p.sel = sel;
     p.k = k;
+    p.n = n;
     p.offset = offset;
+    p.raw_start = raw_start;
     p.window = window;
-    p.scale_log2 = scale * 1.4426950408889634f;
+    p.c = scale * 1.4426950408889634f;
     p.out = static_cast<__nv_bfloat16 *>(out);
+    p.T = static_cast<int>(chunk);
     p.status = status;
-    const int64_t blocks = chunk * (kH / kAttnWarps);
-    attn_warp_kernel<<<static_cast<unsigned>(blocks), kAttnWarps * 32, 0, s>>>(p);
+    const int grid = static_cast<int>(std::min<int64_t>(chunk, std::max(1, sm_count())));
+    attn_kernel<<<grid, kAttnThreads, kAttnSmem, s>>>(tm_q, tm_raw, tm_pool, p);
     return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
@@ -142,6 +513,9 @@ int check_attention(const void *q, const void *raw_kv, int64_t raw_start, int64_
         (pooled_kv && !aligned16(pooled_kv)))
         return DSA_ERR_ARG;
     if (ratio != kRatio || k <= 0 || window <= 0 || !(scale > 0.0f) || isinf(scale))
+        return DSA_ERR_SHAPE;
+    if (chunk * kH > (int64_t{1} << 31) - 1 || raw_rows > (int64_t{1} << 31) - 1 ||
+        n > (int64_t{1} << 31) - 1)
         return DSA_ERR_SHAPE;
     const int64_t first = offset - window + 1 > 0 ? offset - window + 1 : 0;
     if (raw_start > first || raw_start + raw_rows < offset + chunk) return DSA_ERR_RAW_RANGE;

@@ -167,16 +167,18 @@ int dsa_index_score_topk(const void *q_idx, const float *w, const void *pooled_i
  * and the ds4 discussion, Possible design step 4 (selected rows consumed by the
  * indexed attention).
  * Reading taken: for t and head h the keys are the raw rows
- * u = max(0, t-window+1) .. t followed by the pooled rows sel[i, :] that are
- * >= 0; each 512-wide row is both key and value; logits = scale * q . row;
+ * u = max(0, t-window+1) .. t followed by the selected pooled rows; each
+ * 512-wide row is both key and value; logits = scale * q . row;
  * out = softmax-weighted sum of rows, accumulated in fp32, stored bf16.
  *
  *   q [chunk, 64, 512] bf16; raw_kv [raw_rows, 512] bf16 holding absolute raw
  *   rows raw_start .. raw_start+raw_rows-1, which must include
  *   max(0, offset-window+1) .. offset+chunk-1 (else DSA_ERR_RAW_RANGE);
  *   pooled_kv [>= n_pooled, 512] bf16; sel [chunk, index_topk] int32 as written
- *   by dsa_index_score_topk (an entry outside [0, n_vis(t)) other than -1 is
- *   skipped and reported as DSA_ERR_BOUNDS in dev_status);
+ *   by dsa_index_score_topk: row i holds min(index_topk, n_vis(t)) indices
+ *   followed by -1 padding, and only those first min(index_topk, n_vis(t))
+ *   entries are read; among them -1 is skipped, and an index outside
+ *   [0, n_vis(t)) is skipped and reported as DSA_ERR_BOUNDS in dev_status;
  *   window > 0; scale > 0; out [chunk, 64, 512] bf16.
  * Errors: DSA_ERR_ARG, DSA_ERR_SHAPE, DSA_ERR_RAW_RANGE, DSA_ERR_CUDA.
  */
