@@ -30,18 +30,21 @@
 // result (the same max divides out at the end). Output = O^T / sum, bf16.
 #include <math.h>
 
+#include <algorithm>
+
 #include "common.cuh"
 
 namespace dsa {
 
 namespace {
 
-constexpr int kAttnThreads = 192;  // warp 0 TMA, warp 1 MMA + TMEM, warps 2-5 softmax
+constexpr int kAttnThreads = 320;  // warp 0 loader, warp 1 MMA + TMEM, warps 2-9 softmax
+constexpr int kSoftThreads = 256;
 constexpr uint32_t kOffQ = 0;                 // 8 chunks x [64 heads x 128 B]
 constexpr uint32_t kOffKV = 65536;            // 8 chunks x [128 keys x 128 B]
-constexpr uint32_t kOffP = 65536 + 131072;    // [128 keys x 64 heads] bf16, MN-major
-constexpr uint32_t kOffRed = kOffP + 16384;   // [4 warps][64] fp32 block maxima
-constexpr uint32_t kOffL = kOffRed + 1024;    // [4 warps][64] fp32 partial sums
+constexpr uint32_t kOffP = 65536 + 131072;    // P^T [128 keys x 64 heads] bf16; output staging
+constexpr uint32_t kOffRed = kOffP + 16384;   // [4 sub-partitions][64] fp32 block maxima
+constexpr uint32_t kOffL = kOffRed + 1024;    // [4][64] fp32 partial sums
 constexpr uint32_t kOffLinv = kOffL + 1024;   // [64] 1/sum
 constexpr uint32_t kOffM = kOffLinv + 256;    // [2][64] running max (double-buffered)
 constexpr uint32_t kOffAlpha = kOffM + 512;   // [64] rescale factors
@@ -52,6 +55,8 @@ constexpr uint32_t kOCol = 256;  // O^T: 4 d-tiles x 64 columns
 constexpr float kRescale = 8.0f;
 
 struct AttnParams {
+    const __nv_bfloat16 *raw_kv;
+    const __nv_bfloat16 *pooled_kv;
     const int32_t *sel;
     int32_t k;
     int64_t n;
@@ -59,7 +64,6 @@ struct AttnParams {
     int64_t raw_start;
     int32_t window;
     float c;  // softmax scale * log2(e)
-    __nv_bfloat16 *out;
     int T;
     int32_t *status;
 };
@@ -93,11 +97,11 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-// OR of `pred` over the 128 softmax threads (named barrier 1).
-__device__ __forceinline__ bool vote_any_128(bool pred) {
+// OR of `pred` over the 256 softmax threads (named barrier 1).
+__device__ __forceinline__ bool vote_any_soft(bool pred) {
     uint32_t r;
     asm volatile(
-        "{\n .reg .pred p, q;\n setp.ne.b32 p, %1, 0;\n bar.red.or.pred q, 1, 128, p;\n"
+        "{\n .reg .pred p, q;\n setp.ne.b32 p, %1, 0;\n bar.red.or.pred q, 1, 256, p;\n"
         " selp.b32 %0, 1, 0, q;\n}\n"
         : "=r"(r)
         : "r"(static_cast<uint32_t>(pred))
@@ -105,7 +109,25 @@ __device__ __forceinline__ bool vote_any_128(bool pred) {
     return r != 0;
 }
 
-__device__ __forceinline__ void bar_softmax() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+__device__ __forceinline__ void bar_soft() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+
+// Arrive on `bar` once every cp.async this thread issued so far has landed.
+__device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
+}
+
+__device__ __forceinline__ void tma_store_2d(const CUtensorMap *tm, const void *src, int x, int y) {
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                     tm),
+                 "r"(smem_u32(src)), "r"(x), "r"(y)
+                 : "memory");
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
 
 __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
     const uint32_t b = smem_u32(bar);
@@ -115,8 +137,8 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
 }
 
 __global__ void __launch_bounds__(kAttnThreads, 1)
-    attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_raw,
-                const __grid_constant__ CUtensorMap tm_pool, const AttnParams p) {
+    attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_out,
+                const AttnParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -145,12 +167,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
         mbar_init(q_free, 1);
-        for (int c = 0; c < 8; ++c) mbar_init(&kv_full[c], 1);
+        for (int c = 0; c < 8; ++c) mbar_init(&kv_full[c], 32);
         for (int m = 0; m < 4; ++m) mbar_init(&kv_free[m], 1);
         mbar_init(s_full, 1);
-        mbar_init(p_full, 128);
+        mbar_init(p_full, kSoftThreads);
         mbar_init(o_full, 1);
-        mbar_init(o_free, 4);
+        mbar_init(o_free, 8);
         mbar_init(drain, 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -162,9 +184,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     const uint32_t tmem = *tmem_holder;
 
     if (warp == 0) {
-        // ---------------- TMA producer (lane 0 waits and loads tiles; all lanes gather)
+        // ---------------- loader: Q by TMA (lane 0); key rows by cp.async, 8 lanes per
+        // 128-byte row piece, written straight into the 128-byte-swizzled tile
         const uint64_t pol_stream = policy_evict_first();
-        const uint64_t pol_keep = policy_evict_last();
+        const uint32_t kv_base = smem_u32(sKV);
+        const int a = lane >> 3, pc = lane & 7;
         int tok = 0, g = 0, last_q = -1;
         bool ok = true;
         for (int i = blockIdx.x; i < p.T && ok; i += gridDim.x, ++tok) {
@@ -180,49 +204,47 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             }
             ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
             for (int b = 0; b < x.nb && ok; ++b, ++g) {
+                // source row of tile rows lane + 32e; invalid rows read a valid row (masked later)
                 const bool win = b < x.nwb;
-                int y[4] = {0, 0, 0, 0};
-                if (!win) {
-                    const int base = (b - x.nwb) * 128 + lane * 4;
-                    const int32_t *srow = p.sel + static_cast<int64_t>(i) * p.k;
+                int rowi[4];
 #pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const int pos = base + e;
-                        const int32_t j = pos < x.nsel ? __ldg(&srow[pos]) : -1;
+                for (int e = 0; e < 4; ++e) {
+                    const int r = lane + 32 * e;
+                    if (win) {
+                        const int64_t u = min(x.u0 + 128 * b + r, x.t);
+                        rowi[e] = static_cast<int>(u - p.raw_start);
+                    } else {
+                        const int pos = (b - x.nwb) * 128 + r;
+                        const int32_t j =
+                            pos < x.nsel ? __ldg(&p.sel[static_cast<int64_t>(i) * p.k + pos]) : -1;
                         const bool valid = j >= 0 && j < x.nv;
                         if (!valid && j != -1) report(p.status, DSA_ERR_BOUNDS);
-                        y[e] = valid ? j : 0;
+                        rowi[e] = valid ? j : 0;
                     }
                 }
+                const uint8_t *src_base =
+                    reinterpret_cast<const uint8_t *>(win ? p.raw_kv : p.pooled_kv) + pc * 16;
                 for (int m = 0; m < 4 && ok; ++m) {
-                    if (lane == 0) {
-                        ok = mbar_wait(&kv_free[m], (g & 1) ^ 1, abort_flag, p.status);
-                        if (ok) {
-                            mbar_expect_tx(&kv_full[2 * m], 16384);
-                            mbar_expect_tx(&kv_full[2 * m + 1], 16384);
-                            if (win) {
-                                const int row = static_cast<int>(x.u0 + 128 * b - p.raw_start);
-                                for (int c = 2 * m; c < 2 * m + 2; ++c)
-                                    tma_load_2d(sKV + c * 16384, &tm_raw, &kv_full[c], c * 64, row,
-                                                pol_keep);
-                            }
-                        }
-                    }
+                    if (lane == 0) ok = mbar_wait(&kv_free[m], (g & 1) ^ 1, abort_flag, p.status);
                     ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-                    if (ok && !win) {
-                        for (int c = 2 * m; c < 2 * m + 2; ++c)
-                            tma_gather4(sKV + c * 16384 + lane * 512, &tm_pool, &kv_full[c],
-                                        c * 64, y[0], y[1], y[2], y[3], pol_keep);
+                    if (!ok) break;
+#pragma unroll
+                    for (int gq = 0; gq < 32; ++gq) {
+                        const int r = 4 * gq + a;
+                        const int row = __shfl_sync(0xFFFFFFFFu, rowi[gq >> 3], 4 * (gq & 7) + a);
+                        const uint8_t *src = src_base + static_cast<int64_t>(row) * (kD * 2);
+                        const uint32_t dst = kv_base + r * 128 + ((pc ^ (r & 7)) << 4);
+                        cp_async16(dst + (2 * m) * 16384, src + (2 * m) * 128);
+                        cp_async16(dst + (2 * m + 1) * 16384, src + (2 * m + 1) * 128);
                     }
+                    cp_async_arrive(&kv_full[2 * m]);
+                    cp_async_arrive(&kv_full[2 * m + 1]);
                 }
             }
         }
         // no copy into this CTA's shared memory may still be in flight at exit
-        if (lane == 0) {
-            if (g > 0)
-                for (int c = 0; c < 8; ++c) drain_wait(&kv_full[c], (g - 1) & 1);
-            if (last_q >= 0) drain_wait(q_full, last_q & 1);
-        }
+        asm volatile("cp.async.wait_all;" ::: "memory");
+        if (lane == 0 && last_q >= 0) drain_wait(q_full, last_q & 1);
     } else if (warp == 1) {
         // ---------------- MMA issuer
         if (lane == 0) {
@@ -237,6 +259,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 for (int b = 0; b < x.nb && ok; ++b, ++g) {
                     for (int c = 0; c < 8; ++c) {
                         if (!(ok = mbar_wait(&kv_full[c], g & 1, abort_flag, p.status))) break;
+                        // rows landed through the generic proxy; the MMA reads via the async proxy
+                        fence_proxy_async_smem();
                         tc_fence_after();
                         const uint64_t ad = desc_sw128(smem_u32(sKV + c * 16384), 16, 1024);
                         const uint64_t bd = desc_sw128(smem_u32(sQ + c * 8192), 16, 1024);
@@ -271,27 +295,24 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             drain_wait(drain, 0);
         }
     } else {
-        // ---------------- softmax + epilogue: thread owns TMEM lane kl (a key, later a dim)
+        // ---------------- softmax + epilogue, 8 warps: TMEM lanes of sub-partition sp
+        // (keys, later dims) x heads [32*hh, 32*hh+32)
+        const int st = threadIdx.x - 64;
         const int sp = warp & 3;
+        const int hh = (warp - 2) >> 2;
+        const int hb = 32 * hh;
         const int kl = sp * 32 + lane;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(sp * 32) << 16);
+        __nv_bfloat16 *sO = reinterpret_cast<__nv_bfloat16 *>(sP);
         int tok = 0, g = 0, cur = 0;
         for (int i = blockIdx.x; i < p.T; i += gridDim.x, ++tok) {
             const TokenInfo x = token_info(p, i);
-            float l[64];
+            float l[32];
 #pragma unroll
-            for (int h = 0; h < 64; ++h) l[h] = 0.0f;
-            if (kl < 64) sM[cur * 64 + kl] = -INFINITY;
-            bar_softmax();
+            for (int h = 0; h < 32; ++h) l[h] = 0.0f;
+            if (st < 64) sM[cur * 64 + st] = -INFINITY;
+            bar_soft();
             for (int b = 0; b < x.nb; ++b, ++g) {
-                const bool live = mbar_wait(s_full, g & 1, abort_flag, p.status);
-                tc_fence_after();
-                uint32_t sa[32], sb[32];
-                if (live) {
-                    tmem_ld32(lane_base + kSCol, sa);
-                    tmem_ld32(lane_base + kSCol + 32, sb);
-                    tmem_wait_ld();
-                }
                 bool valid;
                 if (b < x.nwb) {
                     valid = x.u0 + 128 * b + kl <= x.t;
@@ -301,88 +322,89 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         pos < x.nsel ? __ldg(&p.sel[static_cast<int64_t>(i) * p.k + pos]) : -1;
                     valid = j >= 0 && j < x.nv;
                 }
+                const bool live = mbar_wait(s_full, g & 1, abort_flag, p.status);
+                tc_fence_after();
+                uint32_t sa[32];
+                if (live) {
+                    tmem_ld32(lane_base + kSCol + hb, sa);
+                    tmem_wait_ld();
+                }
                 valid = valid && live;
-                const float *m_now = sM + cur * 64;
                 bool exceed = false;
+                {
+                    const float *m_now = sM + cur * 64 + hb;
 #pragma unroll
-                for (int h = 0; h < 64; h += 4) {
-                    const float4 m4 = *reinterpret_cast<const float4 *>(&m_now[h]);
-                    const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
-#pragma unroll
-                    for (int e = 0; e < 4; ++e) {
-                        const float s = __uint_as_float(h + e < 32 ? sa[h + e] : sb[h + e - 32]);
-                        exceed |= valid && fmaf(s, p.c, -mm[e]) > kRescale;
+                    for (int h = 0; h < 32; h += 4) {
+                        const float4 m4 = *reinterpret_cast<const float4 *>(&m_now[h]);
+                        exceed |= valid && fmaf(__uint_as_float(sa[h]), p.c, -m4.x) > kRescale;
+                        exceed |= valid && fmaf(__uint_as_float(sa[h + 1]), p.c, -m4.y) > kRescale;
+                        exceed |= valid && fmaf(__uint_as_float(sa[h + 2]), p.c, -m4.z) > kRescale;
+                        exceed |= valid && fmaf(__uint_as_float(sa[h + 3]), p.c, -m4.w) > kRescale;
                     }
                 }
-                if (vote_any_128(exceed)) {
+                if (vote_any_soft(exceed)) {
                     // exact block maxima -> new running max, then rescale sums and O^T
 #pragma unroll
-                    for (int h = 0; h < 64; ++h) {
-                        const float s = __uint_as_float(h < 32 ? sa[h] : sb[h - 32]);
-                        const float wm = redux_max(valid ? s * p.c : -INFINITY);
-                        if (lane == (h & 31)) sRed[sp * 64 + h] = wm;
+                    for (int h = 0; h < 32; ++h) {
+                        const float wm =
+                            redux_max(valid ? __uint_as_float(sa[h]) * p.c : -INFINITY);
+                        if (lane == h) sRed[sp * 64 + hb + h] = wm;
                     }
-                    bar_softmax();
-                    if (kl < 64) {
-                        const float bm = fmaxf(fmaxf(sRed[kl], sRed[64 + kl]),
-                                               fmaxf(sRed[128 + kl], sRed[192 + kl]));
-                        const float m_old = sM[cur * 64 + kl];
+                    bar_soft();
+                    if (st < 64) {
+                        const float bm = fmaxf(fmaxf(sRed[st], sRed[64 + st]),
+                                               fmaxf(sRed[128 + st], sRed[192 + st]));
+                        const float m_old = sM[cur * 64 + st];
                         const float m_new = fmaxf(m_old, bm);
-                        sM[(cur ^ 1) * 64 + kl] = m_new;
-                        sAlpha[kl] = ex2(m_old - m_new);
+                        sM[(cur ^ 1) * 64 + st] = m_new;
+                        sAlpha[st] = ex2(m_old - m_new);
                     }
-                    bar_softmax();
+                    bar_soft();
                     cur ^= 1;
 #pragma unroll
-                    for (int h = 0; h < 64; h += 4) {
-                        const float4 a4 = *reinterpret_cast<const float4 *>(&sAlpha[h]);
-                        l[h] *= a4.x;
-                        l[h + 1] *= a4.y;
-                        l[h + 2] *= a4.z;
-                        l[h + 3] *= a4.w;
-                    }
+                    for (int h = 0; h < 32; ++h) l[h] *= sAlpha[hb + h];
                     if (b > 0 && live) {
 #pragma unroll 1
-                        for (int c32 = 0; c32 < 8; ++c32) {
+                        for (int m = 0; m < 4; ++m) {
                             uint32_t oa[32];
-                            const uint32_t col = lane_base + kOCol + 32 * c32;
-                            const float *al = sAlpha + (c32 & 1) * 32;
+                            const uint32_t col = lane_base + kOCol + 64 * m + hb;
                             tmem_ld32(col, oa);
                             tmem_wait_ld();
 #pragma unroll
                             for (int h = 0; h < 32; ++h)
-                                oa[h] = __float_as_uint(__uint_as_float(oa[h]) * al[h]);
+                                oa[h] = __float_as_uint(__uint_as_float(oa[h]) * sAlpha[hb + h]);
                             tmem_st32(col, oa);
                         }
                         tmem_wait_st();
                     }
                 }
-                // P^T row for this key: 64 heads, bf16, 128-byte swizzled row
-                const float *m_use = sM + cur * 64;
-                uint8_t *prow = sP + kl * 128;
+                // this thread's 32 heads of the P^T row for key kl: 4 swizzled 16-byte pieces
+                {
+                    const float *m_use = sM + cur * 64 + hb;
+                    uint8_t *prow = sP + kl * 128;
 #pragma unroll
-                for (int q = 0; q < 8; ++q) {
-                    uint32_t pk[4];
+                    for (int q = 0; q < 4; ++q) {
+                        uint32_t pk[4];
 #pragma unroll
-                    for (int h2 = 0; h2 < 8; h2 += 4) {
-                        const int h = 8 * q + h2;
-                        const float4 m4 = *reinterpret_cast<const float4 *>(&m_use[h]);
-                        const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
-                        float pr[4];
+                        for (int h2 = 0; h2 < 8; h2 += 4) {
+                            const int h = 8 * q + h2;
+                            const float4 m4 = *reinterpret_cast<const float4 *>(&m_use[h]);
+                            const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
+                            float pr[4];
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float sv =
-                                __uint_as_float(h + e < 32 ? sa[h + e] : sb[h + e - 32]);
-                            pr[e] = valid ? ex2(fmaf(sv, p.c, -mm[e])) : 0.0f;
-                            l[h + e] += pr[e];
+                            for (int e = 0; e < 4; ++e) {
+                                pr[e] = valid ? ex2(fmaf(__uint_as_float(sa[h + e]), p.c, -mm[e]))
+                                              : 0.0f;
+                                l[h + e] += pr[e];
+                            }
+                            const __nv_bfloat162 v0 = __floats2bfloat162_rn(pr[0], pr[1]);
+                            const __nv_bfloat162 v1 = __floats2bfloat162_rn(pr[2], pr[3]);
+                            pk[h2 / 2] = *reinterpret_cast<const uint32_t *>(&v0);
+                            pk[h2 / 2 + 1] = *reinterpret_cast<const uint32_t *>(&v1);
                         }
-                        const __nv_bfloat162 v0 = __floats2bfloat162_rn(pr[0], pr[1]);
-                        const __nv_bfloat162 v1 = __floats2bfloat162_rn(pr[2], pr[3]);
-                        pk[h2 / 2] = *reinterpret_cast<const uint32_t *>(&v0);
-                        pk[h2 / 2 + 1] = *reinterpret_cast<const uint32_t *>(&v1);
+                        *reinterpret_cast<uint4 *>(prow + (((4 * hh + q) ^ (kl & 7)) << 4)) =
+                            make_uint4(pk[0], pk[1], pk[2], pk[3]);
                     }
-                    *reinterpret_cast<uint4 *>(prow + ((q ^ (kl & 7)) << 4)) =
-                        make_uint4(pk[0], pk[1], pk[2], pk[3]);
                 }
                 fence_proxy_async_smem();
                 tc_fence_before();
@@ -391,70 +413,71 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             // ---- token end: sums over keys, then O^T / sum -> out[t, h, d]
             const bool live = mbar_wait(o_full, tok & 1, abort_flag, p.status);
             tc_fence_after();
-            // transpose-reduce the 64 partial sums across the warp: lane ends
-            // with the warp's totals for heads 2*lane and 2*lane+1
-            {
-                float *v = l;
+            // transpose-reduce the 32 partial sums across the warp: lane ends with
+            // the warp's total for head hb + lane
 #pragma unroll
-                for (int i2 = 0; i2 < 32; ++i2) {
-                    const bool hi = lane & 16;
-                    const float send = hi ? v[i2] : v[i2 + 32];
-                    const float keep = hi ? v[i2 + 32] : v[i2];
-                    v[i2] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 16);
-                }
-#pragma unroll
-                for (int i2 = 0; i2 < 16; ++i2) {
-                    const bool hi = lane & 8;
-                    const float send = hi ? v[i2] : v[i2 + 16];
-                    const float keep = hi ? v[i2 + 16] : v[i2];
-                    v[i2] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 8);
-                }
-#pragma unroll
-                for (int i2 = 0; i2 < 8; ++i2) {
-                    const bool hi = lane & 4;
-                    const float send = hi ? v[i2] : v[i2 + 8];
-                    const float keep = hi ? v[i2 + 8] : v[i2];
-                    v[i2] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 4);
-                }
-#pragma unroll
-                for (int i2 = 0; i2 < 4; ++i2) {
-                    const bool hi = lane & 2;
-                    const float send = hi ? v[i2] : v[i2 + 4];
-                    const float keep = hi ? v[i2 + 4] : v[i2];
-                    v[i2] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 2);
-                }
-#pragma unroll
-                for (int i2 = 0; i2 < 2; ++i2) {
-                    const bool hi = lane & 1;
-                    const float send = hi ? v[i2] : v[i2 + 2];
-                    const float keep = hi ? v[i2 + 2] : v[i2];
-                    v[i2] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 1);
-                }
-                *reinterpret_cast<float2 *>(&sL[sp * 64 + 2 * lane]) = make_float2(v[0], v[1]);
+            for (int i2 = 0; i2 < 16; ++i2) {
+                const bool hi = lane & 16;
+                const float send = hi ? l[i2] : l[i2 + 16];
+                const float keep = hi ? l[i2 + 16] : l[i2];
+                l[i2] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 16);
             }
-            bar_softmax();
-            if (kl < 64)
-                sLinv[kl] = 1.0f / (sL[kl] + sL[64 + kl] + sL[128 + kl] + sL[192 + kl]);
-            bar_softmax();
-            if (live) {
-                __nv_bfloat16 *orow = p.out + static_cast<int64_t>(i) * (kH * kD);
+#pragma unroll
+            for (int i2 = 0; i2 < 8; ++i2) {
+                const bool hi = lane & 8;
+                const float send = hi ? l[i2] : l[i2 + 8];
+                const float keep = hi ? l[i2 + 8] : l[i2];
+                l[i2] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 8);
+            }
+#pragma unroll
+            for (int i2 = 0; i2 < 4; ++i2) {
+                const bool hi = lane & 4;
+                const float send = hi ? l[i2] : l[i2 + 4];
+                const float keep = hi ? l[i2 + 4] : l[i2];
+                l[i2] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 4);
+            }
+#pragma unroll
+            for (int i2 = 0; i2 < 2; ++i2) {
+                const bool hi = lane & 2;
+                const float send = hi ? l[i2] : l[i2 + 2];
+                const float keep = hi ? l[i2 + 2] : l[i2];
+                l[i2] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 2);
+            }
+            {
+                const bool hi = lane & 1;
+                const float send = hi ? l[0] : l[1];
+                const float keep = hi ? l[1] : l[0];
+                l[0] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 1);
+            }
+            sL[sp * 64 + hb + lane] = l[0];
+            bar_soft();
+            if (st < 64) sLinv[st] = 1.0f / (sL[st] + sL[64 + st] + sL[128 + st] + sL[192 + st]);
+            bar_soft();
+            // four [64 heads x 128 dims] tiles staged in sP, each written by one TMA store
 #pragma unroll 1
-                for (int c32 = 0; c32 < 8; ++c32) {
+            for (int m = 0; m < 4; ++m) {
+                if (st == 0 && m > 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+                bar_soft();
+                if (live) {
                     uint32_t oa[32];
-                    tmem_ld32(lane_base + kOCol + 32 * c32, oa);
+                    tmem_ld32(lane_base + kOCol + 64 * m + hb, oa);
                     tmem_wait_ld();
-                    const int d = 128 * (c32 >> 1) + kl;
-                    const int h0 = (c32 & 1) * 32;
 #pragma unroll
                     for (int h = 0; h < 32; ++h)
-                        orow[(h0 + h) * kD + d] =
-                            __float2bfloat16_rn(__uint_as_float(oa[h]) * sLinv[h0 + h]);
+                        sO[(hb + h) * 128 + kl] =
+                            __float2bfloat16_rn(__uint_as_float(oa[h]) * sLinv[hb + h]);
                 }
+                fence_proxy_async_smem();
+                bar_soft();
+                if (st == 0 && live) tma_store_2d(&tm_out, sP, 128 * m, i * 64);
             }
+            // sP is reused for P^T by the next token: its last store must have read it
+            if (st == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(o_free);
         }
+        if (st == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     }
     __syncthreads();
     if (warp == 1) {
@@ -470,6 +493,7 @@ int launch_attention(const void *q, const void *raw_kv, int64_t raw_start, int64
                      const void *pooled_kv, int64_t n, const int32_t *sel, int32_t k,
                      int64_t chunk, int64_t offset, int32_t window, float scale, void *out,
                      int32_t *status, cudaStream_t s) {
+    (void)raw_rows;
     static bool attr_set = false;
     if (!attr_set) {
         if (cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -477,16 +501,15 @@ int launch_attention(const void *q, const void *raw_kv, int64_t raw_start, int64
             return DSA_ERR_CUDA;
         attr_set = true;
     }
-    CUtensorMap tm_q, tm_raw, tm_pool;
+    CUtensorMap tm_q, tm_out;
     if (!make_tmap_bf16(&tm_q, q, kD, static_cast<uint64_t>(chunk) * kH, kD * 2, 64, 64))
         return DSA_ERR_CUDA;
-    if (!make_tmap_bf16(&tm_raw, raw_kv, kD, static_cast<uint64_t>(raw_rows), kD * 2, 64, 128))
+    if (!make_tmap_bf16(&tm_out, out, kD, static_cast<uint64_t>(chunk) * kH, kD * 2, 128, 64,
+                        false))
         return DSA_ERR_CUDA;
-    // with no pooled rows the gather map is never used; point it at raw_kv
-    const void *pool_base = n > 0 ? pooled_kv : raw_kv;
-    const uint64_t pool_rows = n > 0 ? static_cast<uint64_t>(n) : static_cast<uint64_t>(raw_rows);
-    if (!make_tmap_bf16(&tm_pool, pool_base, kD, pool_rows, kD * 2, 64, 1)) return DSA_ERR_CUDA;
     AttnParams p;
+    p.raw_kv = static_cast<const __nv_bfloat16 *>(raw_kv);
+    p.pooled_kv = static_cast<const __nv_bfloat16 *>(pooled_kv);
     p.sel = sel;
     p.k = k;
     p.n = n;
@@ -494,11 +517,10 @@ int launch_attention(const void *q, const void *raw_kv, int64_t raw_start, int64
     p.raw_start = raw_start;
     p.window = window;
     p.c = scale * 1.4426950408889634f;
-    p.out = static_cast<__nv_bfloat16 *>(out);
     p.T = static_cast<int>(chunk);
     p.status = status;
     const int grid = static_cast<int>(std::min<int64_t>(chunk, std::max(1, sm_count())));
-    attn_kernel<<<grid, kAttnThreads, kAttnSmem, s>>>(tm_q, tm_raw, tm_pool, p);
+    attn_kernel<<<grid, kAttnThreads, kAttnSmem, s>>>(tm_q, tm_out, p);
     return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 

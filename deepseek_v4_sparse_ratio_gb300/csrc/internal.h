@@ -31,11 +31,12 @@ inline int64_t n_visible(int64_t t, int64_t n) {
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
-// 2-D bf16 tensor map with 128-byte swizzle: `inner` elements per row (the
-// contiguous dimension), `rows` rows of `row_bytes` each, box of
-// box_inner x box_rows. Returns false if the driver rejects it.
+// 2-D bf16 tensor map: `inner` elements per row (the contiguous dimension),
+// `rows` rows of `row_bytes` each, box of box_inner x box_rows, 128-byte
+// swizzle or none. Returns false if the driver rejects it.
 bool make_tmap_bf16(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
-                    uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows);
+                    uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows,
+                    bool swizzle128 = true);
 
 int sm_count();
 

@@ -145,7 +145,7 @@ std::once_flag g_encode_once;
 }  // namespace
 
 bool make_tmap_bf16(CUtensorMap *map, const void *base, uint64_t inner, uint64_t rows,
-                    uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows) {
+                    uint64_t row_bytes, uint32_t box_inner, uint32_t box_rows, bool swizzle128) {
     std::call_once(g_encode_once, [] {
         void *fn = nullptr;
         cudaDriverEntryPointQueryResult q;
@@ -161,7 +161,8 @@ bool make_tmap_bf16(CUtensorMap *map, const void *base, uint64_t inner, uint64_t
     cuuint32_t estr[2] = {1, 1};
     CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
                           strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
-                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          swizzle128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_NONE,
+                          CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                           CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
     return r == CUDA_SUCCESS;
 }
