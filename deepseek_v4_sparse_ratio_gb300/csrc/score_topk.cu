@@ -308,6 +308,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 constexpr int kTopkThreads = 512;
 constexpr int kTopkWarps = kTopkThreads / 32;
 constexpr int kStageMaxFloats = 49152;  // rows up to this long are staged in shared memory
+constexpr int kBins = 2048;
+constexpr int kCandCap = 4096;
 
 __device__ __forceinline__ uint32_t order_key(float f) {
     const uint32_t b = __float_as_uint(f);
@@ -344,15 +346,70 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *warp_s
     return r;
 }
 
+// After hist[0..nb) is filled: the bin b holding the `need`-th largest element
+// (counting from the top bin down) and how many elements lie in higher bins.
+__device__ __forceinline__ void find_bin(const uint32_t *hist, int nb, uint32_t need,
+                                         uint32_t *warp_sums, uint32_t *s_bin, uint32_t *s_above) {
+    const int per = nb / kTopkThreads;
+    const int top = nb - per * threadIdx.x;  // thread i owns bins [top-per, top)
+    uint32_t mine = 0;
+    for (int b = top - per; b < top; ++b) mine += hist[b];
+    uint32_t tot;
+    uint32_t cum = block_excl_scan(mine, warp_sums, &tot);
+    for (int b = top - 1; b >= top - per; --b) {
+        const uint32_t c = hist[b];
+        if (cum < need && need <= cum + c) {
+            *s_bin = static_cast<uint32_t>(b);
+            *s_above = cum;
+        }
+        cum += c;
+    }
+    __syncthreads();
+}
+
+// Radix select over `count` order keys given by key_at(i): the key of the
+// need-th largest element and how many elements equal to it are kept
+// (11/11/10-bit digits from the top).
+template <typename KeyAt>
+__device__ __forceinline__ void radix_select(KeyAt key_at, int64_t count, uint32_t need,
+                                             uint32_t *hist, uint32_t *warp_sums, uint32_t *s_bin,
+                                             uint32_t *s_above, uint32_t *thr_out,
+                                             uint32_t *need_out) {
+    uint32_t prefix = 0;
+    for (int pass = 0; pass < 3; ++pass) {
+        const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+        const int bits = pass == 2 ? 10 : 11;
+        const int nb = 1 << bits;
+        for (int i = threadIdx.x; i < nb; i += kTopkThreads) hist[i] = 0;
+        __syncthreads();
+        for (int64_t j = threadIdx.x; j < count; j += kTopkThreads) {
+            const uint32_t u = key_at(j);
+            if (pass == 0 || (u >> (shift + bits)) == prefix)
+                atomicAdd(&hist[(u >> shift) & (nb - 1)], 1u);
+        }
+        __syncthreads();
+        find_bin(hist, nb, need, warp_sums, s_bin, s_above);
+        prefix = (prefix << bits) | *s_bin;
+        need -= *s_above;
+        __syncthreads();
+    }
+    *thr_out = prefix;
+    *need_out = need;
+}
+
 template <bool kStaged>
 __global__ void __launch_bounds__(kTopkThreads)
     topk_kernel(const float *__restrict__ scores, int64_t stride, int64_t n, int64_t offset,
                 int64_t r0, int32_t k, int32_t *__restrict__ sel) {
     extern __shared__ float srow[];
-    __shared__ uint32_t hist[2048];
+    __shared__ uint32_t hist[kBins];
+    __shared__ uint32_t cand[kCandCap];
     __shared__ uint32_t warp_sums[kTopkWarps + 1];
-    __shared__ uint32_t s_digit, s_above;
+    __shared__ uint32_t s_bin, s_above, s_cnt;
+    __shared__ float s_min[kTopkWarps], s_max[kTopkWarps];
+    __shared__ uint32_t w_gt[kTopkWarps], w_eq[kTopkWarps];
 
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int row = blockIdx.x;
     const int64_t t = offset + r0 + row;
     const int64_t L = min(n, (t + 1) / kRatio);
@@ -371,64 +428,100 @@ __global__ void __launch_bounds__(kTopkThreads)
         src = srow;
     }
 
-    // ---- radix select of the k-th largest key: digits [31:21], [20:10], [9:0]
-    uint32_t prefix = 0;
-    uint32_t need = static_cast<uint32_t>(k);
-    for (int pass = 0; pass < 3; ++pass) {
-        const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
-        const int bits = pass == 2 ? 10 : 11;
-        const int nb = 1 << bits;
-        for (int i = threadIdx.x; i < nb; i += kTopkThreads) hist[i] = 0;
-        __syncthreads();
-        for (int64_t j = threadIdx.x; j < L; j += kTopkThreads) {
-            const uint32_t u = order_key(src[j]);
-            if (pass == 0 || (u >> (shift + bits)) == prefix)
-                atomicAdd(&hist[(u >> shift) & (nb - 1)], 1u);
-        }
-        __syncthreads();
-        // thread i owns bins [hi-per*(i+1), hi-per*i): descending order over threads
-        const int per = nb / kTopkThreads;
-        const int top = nb - per * threadIdx.x;  // exclusive upper bin
-        uint32_t mine = 0;
-        for (int b = top - per; b < top; ++b) mine += hist[b];
-        uint32_t tot;
-        const uint32_t above_mine = block_excl_scan(mine, warp_sums, &tot);
-        uint32_t cum = above_mine;
-        for (int b = top - 1; b >= top - per; --b) {
-            const uint32_t c = hist[b];
-            if (cum < need && need <= cum + c) {
-                s_digit = static_cast<uint32_t>(b);
-                s_above = cum;
-            }
-            cum += c;
-        }
-        __syncthreads();
-        prefix = (prefix << bits) | s_digit;
-        need -= s_above;
-        __syncthreads();
+    // ---- 1. range of the row
+    float vmin = INFINITY, vmax = -INFINITY;
+    for (int64_t j = threadIdx.x; j < L; j += kTopkThreads) {
+        const float v = src[j];
+        vmin = fminf(vmin, v);
+        vmax = fmaxf(vmax, v);
     }
-    const uint32_t thr = prefix;  // key of the k-th largest score
-    // `need` equal keys are kept, lowest indices first
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        vmin = fminf(vmin, __shfl_xor_sync(0xFFFFFFFFu, vmin, o));
+        vmax = fmaxf(vmax, __shfl_xor_sync(0xFFFFFFFFu, vmax, o));
+    }
+    if (lane == 0) {
+        s_min[warp] = vmin;
+        s_max[warp] = vmax;
+    }
+    for (int i = threadIdx.x; i < kBins; i += kTopkThreads) hist[i] = 0;
+    if (threadIdx.x == 0) s_cnt = 0;
+    __syncthreads();
+    vmin = s_min[0];
+    vmax = s_max[0];
+#pragma unroll
+    for (int w = 1; w < kTopkWarps; ++w) {
+        vmin = fminf(vmin, s_min[w]);
+        vmax = fmaxf(vmax, s_max[w]);
+    }
 
-    // ---- emit kept indices in ascending order
-    uint32_t run_sel = 0, run_eq = 0;
-    for (int64_t base = 0; base < L; base += kTopkThreads) {
-        const int64_t j = base + threadIdx.x;
-        uint32_t gt = 0, eq = 0;
-        if (j < L) {
-            const uint32_t u = order_key(src[j]);
-            gt = u > thr;
-            eq = u == thr;
+    uint32_t thr, need_eq;
+    if (vmin == vmax) {
+        // every visible score is equal: the k lowest indices
+        thr = order_key(vmax);
+        need_eq = static_cast<uint32_t>(k);
+    } else {
+        // ---- 2. linear bins between min and max: a monotone map, so every element
+        // of a higher bin is >= every element of a lower bin
+        const float scale = static_cast<float>(kBins) / (vmax - vmin);
+        auto bin_of = [&](float v) { return min(kBins - 1, static_cast<int>((v - vmin) * scale)); };
+        for (int64_t j = threadIdx.x; j < L; j += kTopkThreads) atomicAdd(&hist[bin_of(src[j])], 1u);
+        __syncthreads();
+        find_bin(hist, kBins, static_cast<uint32_t>(k), warp_sums, &s_bin, &s_above);
+        const int bstar = static_cast<int>(s_bin);
+        const uint32_t need = static_cast<uint32_t>(k) - s_above;
+        // ---- 3. exact selection among the threshold bin's elements
+        for (int64_t j = threadIdx.x; j < L; j += kTopkThreads) {
+            const float v = src[j];
+            if (bin_of(v) == bstar) {
+                const uint32_t c = atomicAdd(&s_cnt, 1u);
+                if (c < kCandCap) cand[c] = order_key(v);
+            }
         }
-        uint32_t tot;
-        const uint32_t ex = block_excl_scan((eq << 16) | gt, warp_sums, &tot);
-        const uint32_t gt_before = ex & 0xFFFFu, eq_before = ex >> 16;
-        const uint32_t eq_taken_before = min(run_eq + eq_before, need) - min(run_eq, need);
-        const bool take = gt || (eq && run_eq + eq_before < need);
-        if (take) out[run_sel + gt_before + eq_taken_before] = static_cast<int32_t>(j);
-        const uint32_t gt_tot = tot & 0xFFFFu, eq_tot = tot >> 16;
-        run_sel += gt_tot + (min(run_eq + eq_tot, need) - min(run_eq, need));
-        run_eq += eq_tot;
+        __syncthreads();
+        const uint32_t cnt = s_cnt;
+        if (cnt <= kCandCap) {
+            radix_select([&](int64_t j) { return cand[j]; }, cnt, need, hist, warp_sums, &s_bin,
+                         &s_above, &thr, &need_eq);
+        } else {
+            radix_select([&](int64_t j) { return order_key(src[j]); }, L, static_cast<uint32_t>(k),
+                         hist, warp_sums, &s_bin, &s_above, &thr, &need_eq);
+        }
+    }
+
+    // ---- 4. emit kept indices ascending: each warp owns a contiguous segment
+    const int64_t seg = ((L + kTopkWarps - 1) / kTopkWarps + 31) / 32 * 32;
+    const int64_t lo = min(L, seg * warp), hi = min(L, seg * (warp + 1));
+    uint32_t ngt = 0, neq = 0;
+    for (int64_t base = lo; base < hi; base += 32) {
+        const int64_t j = base + lane;
+        const uint32_t u = j < hi ? order_key(src[j]) : 0u;
+        ngt += __popc(__ballot_sync(0xFFFFFFFFu, j < hi && u > thr));
+        neq += __popc(__ballot_sync(0xFFFFFFFFu, j < hi && u == thr));
+    }
+    if (lane == 0) {
+        w_gt[warp] = ngt;
+        w_eq[warp] = neq;
+    }
+    __syncthreads();
+    uint32_t base_gt = 0, base_eq = 0;
+    for (int w = 0; w < warp; ++w) {
+        base_gt += w_gt[w];
+        base_eq += w_eq[w];
+    }
+    const uint32_t lt_mask = (1u << lane) - 1u;
+    for (int64_t base = lo; base < hi; base += 32) {
+        const int64_t j = base + lane;
+        const uint32_t u = j < hi ? order_key(src[j]) : 0u;
+        const bool gt = j < hi && u > thr;
+        const bool eq = j < hi && u == thr;
+        const uint32_t mg = __ballot_sync(0xFFFFFFFFu, gt);
+        const uint32_t me = __ballot_sync(0xFFFFFFFFu, eq);
+        const uint32_t eq_before = base_eq + __popc(me & lt_mask);
+        if (gt || (eq && eq_before < need_eq))
+            out[base_gt + __popc(mg & lt_mask) + min(eq_before, need_eq)] = static_cast<int32_t>(j);
+        base_gt += __popc(mg);
+        base_eq += __popc(me);
     }
 }
 
