@@ -38,7 +38,17 @@ namespace dsa {
 
 namespace {
 
-constexpr int kAttnThreads = 320;  // warp 0 loader, warp 1 MMA + TMEM, warps 2-9 softmax
+// Warpgroups 0-1: loader warps 0-6 and the MMA warp 7; warpgroups 2-3: softmax
+// warps 8-15. setmaxnreg moves registers from the first two warpgroups to the
+// softmax ones: 256*80 + 256*176 = 512*128, the launch allocation (checked on
+// the host before the first launch).
+constexpr int kLoadWarps = 7;
+constexpr int kMmaWarp = 7;
+constexpr int kSoftWarp0 = 8;
+constexpr int kAttnThreads = 512;
+constexpr int kRegsLaunch = 128;
+constexpr int kRegsLow = 80;
+constexpr int kRegsSoft = 176;
 constexpr int kSoftThreads = 256;
 constexpr uint32_t kOffQ = 0;                 // 8 chunks x [64 heads x 128 B]
 constexpr uint32_t kOffKV = 65536;            // 8 chunks x [128 keys x 128 B]
@@ -167,7 +177,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
         mbar_init(q_free, 1);
-        for (int c = 0; c < 8; ++c) mbar_init(&kv_full[c], 32);
+        for (int c = 0; c < 8; ++c) mbar_init(&kv_full[c], 32 * kLoadWarps);  // noinc arrivals
         for (int m = 0; m < 4; ++m) mbar_init(&kv_free[m], 1);
         mbar_init(s_full, 1);
         mbar_init(p_full, kSoftThreads);
@@ -177,23 +187,51 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         *abort_flag = 0;
         fence_barrier_init();
     }
-    if (warp == 1) tmem_alloc(tmem_holder, 512);
+    if (warp == kMmaWarp) tmem_alloc(tmem_holder, 512);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
-    if (warp == 0) {
-        // ---------------- loader: Q by TMA (lane 0); key rows by cp.async, 8 lanes per
-        // 128-byte row piece, written straight into the 128-byte-swizzled tile
+    if (warp < kSoftWarp0) {
+      // warpgroups 0-1 give registers to the softmax warpgroups (one instruction
+      // instance for all eight warps)
+      asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
+      if (warp < kLoadWarps) {
+        // ---------------- loaders: Q by TMA (warp 0, lane 0); key rows by cp.async, 8
+        // lanes per 128-byte row piece, written straight into the 128-byte-swizzled tile.
+        // Loader lw copies the 4-row groups lw, lw+7, lw+14, ... (at most 5, 20 rows).
+        // Each block's selection entries are read one block ahead.
+        const int lw = warp;
         const uint64_t pol_stream = policy_evict_first();
         const uint32_t kv_base = smem_u32(sKV);
         const int a = lane >> 3, pc = lane & 7;
+        const int ngroups = (32 - lw + kLoadWarps - 1) / kLoadWarps;
+        const bool holder = lane < 4 * ngroups;
+        const int r_tile = 4 * (lw + kLoadWarps * (lane >> 2)) + (lane & 3);  // if holder
+        auto fetch = [&](const TokenInfo &x, int i, int b) -> int32_t {
+            const int pos = (b - x.nwb) * 128 + r_tile;
+            return (holder && b >= x.nwb && pos < x.nsel)
+                       ? __ldg(&p.sel[static_cast<int64_t>(i) * p.k + pos])
+                       : -1;
+        };
+        auto row_of = [&](const TokenInfo &x, int b, int32_t j) -> int {
+            if (b < x.nwb) {
+                const int64_t u = min(x.u0 + 128 * b + r_tile, x.t);
+                return static_cast<int>(u - p.raw_start);
+            }
+            const bool valid = j >= 0 && j < x.nv;
+            const int pos = (b - x.nwb) * 128 + r_tile;
+            if (holder && !valid && j != -1 && pos < x.nsel) report(p.status, DSA_ERR_BOUNDS);
+            return valid ? j : 0;
+        };
         int tok = 0, g = 0, last_q = -1;
         bool ok = true;
-        for (int i = blockIdx.x; i < p.T && ok; i += gridDim.x, ++tok) {
-            const TokenInfo x = token_info(p, i);
-            if (lane == 0) {
+        int i = blockIdx.x;
+        TokenInfo x = token_info(p, i < p.T ? i : 0);
+        int32_t jn = i < p.T ? fetch(x, i, 0) : -1;
+        for (; i < p.T && ok; i += gridDim.x, ++tok) {
+            if (lw == 0 && lane == 0) {
                 ok = mbar_wait(q_free, (tok & 1) ^ 1, abort_flag, p.status);
                 if (ok) {
                     mbar_expect_tx(q_full, 65536);
@@ -203,50 +241,39 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 }
             }
             ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+            const int inext = i + static_cast<int>(gridDim.x);
+            const TokenInfo xnext = token_info(p, inext < p.T ? inext : i);
             for (int b = 0; b < x.nb && ok; ++b, ++g) {
-                // source row of tile rows lane + 32e; invalid rows read a valid row (masked later)
-                const bool win = b < x.nwb;
-                int rowi[4];
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const int r = lane + 32 * e;
-                    if (win) {
-                        const int64_t u = min(x.u0 + 128 * b + r, x.t);
-                        rowi[e] = static_cast<int>(u - p.raw_start);
-                    } else {
-                        const int pos = (b - x.nwb) * 128 + r;
-                        const int32_t j =
-                            pos < x.nsel ? __ldg(&p.sel[static_cast<int64_t>(i) * p.k + pos]) : -1;
-                        const bool valid = j >= 0 && j < x.nv;
-                        if (!valid && j != -1) report(p.status, DSA_ERR_BOUNDS);
-                        rowi[e] = valid ? j : 0;
-                    }
-                }
+                const int row = row_of(x, b, jn);
                 const uint8_t *src_base =
-                    reinterpret_cast<const uint8_t *>(win ? p.raw_kv : p.pooled_kv) + pc * 16;
+                    reinterpret_cast<const uint8_t *>(b < x.nwb ? p.raw_kv : p.pooled_kv) + pc * 16;
                 for (int m = 0; m < 4 && ok; ++m) {
                     if (lane == 0) ok = mbar_wait(&kv_free[m], (g & 1) ^ 1, abort_flag, p.status);
                     ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
                     if (!ok) break;
-#pragma unroll
-                    for (int gq = 0; gq < 32; ++gq) {
-                        const int r = 4 * gq + a;
-                        const int row = __shfl_sync(0xFFFFFFFFu, rowi[gq >> 3], 4 * (gq & 7) + a);
-                        const uint8_t *src = src_base + static_cast<int64_t>(row) * (kD * 2);
+#pragma unroll 1
+                    for (int gq = 0; gq < ngroups; ++gq) {
+                        const int r = 4 * (lw + kLoadWarps * gq) + a;
+                        const int srow = __shfl_sync(0xFFFFFFFFu, row, 4 * gq + a);
+                        const uint8_t *src = src_base + static_cast<int64_t>(srow) * (kD * 2);
                         const uint32_t dst = kv_base + r * 128 + ((pc ^ (r & 7)) << 4);
                         cp_async16(dst + (2 * m) * 16384, src + (2 * m) * 128);
                         cp_async16(dst + (2 * m + 1) * 16384, src + (2 * m + 1) * 128);
                     }
                     cp_async_arrive(&kv_full[2 * m]);
                     cp_async_arrive(&kv_full[2 * m + 1]);
+                    if (m == 0)
+                        jn = (b + 1 < x.nb) ? fetch(x, i, b + 1)
+                                            : (inext < p.T ? fetch(xnext, inext, 0) : -1);
                 }
             }
+            x = xnext;
         }
         // no copy into this CTA's shared memory may still be in flight at exit
         asm volatile("cp.async.wait_all;" ::: "memory");
-        if (lane == 0 && last_q >= 0) drain_wait(q_full, last_q & 1);
-    } else if (warp == 1) {
-        // ---------------- MMA issuer
+        if (lw == 0 && lane == 0 && last_q >= 0) drain_wait(q_full, last_q & 1);
+      } else {
+        // ---------------- MMA issuer (warp 7)
         if (lane == 0) {
             constexpr uint32_t idesc_qk = idesc_bf16(128, 64, false, false);
             constexpr uint32_t idesc_pv = idesc_bf16(128, 64, true, true);
@@ -257,6 +284,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 if (!(ok = mbar_wait(q_full, tok & 1, abort_flag, p.status))) break;
                 tc_fence_after();
                 for (int b = 0; b < x.nb && ok; ++b, ++g) {
+#pragma unroll 1
                     for (int c = 0; c < 8; ++c) {
                         if (!(ok = mbar_wait(&kv_full[c], g & 1, abort_flag, p.status))) break;
                         // rows landed through the generic proxy; the MMA reads via the async proxy
@@ -278,6 +306,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         if (!(ok = mbar_wait(o_free, (tok - 1) & 1, abort_flag, p.status))) break;
                         tc_fence_after();
                     }
+#pragma unroll 1
                     for (int m = 0; m < 4; ++m) {
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk) {
@@ -294,12 +323,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             mma_commit(drain);
             drain_wait(drain, 0);
         }
+      }
     } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoft));
         // ---------------- softmax + epilogue, 8 warps: TMEM lanes of sub-partition sp
         // (keys, later dims) x heads [32*hh, 32*hh+32)
-        const int st = threadIdx.x - 64;
+        const int st = threadIdx.x - 32 * kSoftWarp0;
         const int sp = warp & 3;
-        const int hh = (warp - 2) >> 2;
+        const int hh = (warp - kSoftWarp0) >> 2;
         const int hb = 32 * hh;
         const int kl = sp * 32 + lane;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(sp * 32) << 16);
@@ -480,7 +511,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (st == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     }
     __syncthreads();
-    if (warp == 1) {
+    if (warp == kMmaWarp) {
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, 512);
@@ -494,12 +525,16 @@ int launch_attention(const void *q, const void *raw_kv, int64_t raw_start, int64
                      int64_t chunk, int64_t offset, int32_t window, float scale, void *out,
                      int32_t *status, cudaStream_t s) {
     (void)raw_rows;
-    static bool attr_set = false;
-    if (!attr_set) {
+    static bool checked = false;
+    if (!checked) {
+        // the setmaxnreg split is only safe with the launch allocation it assumes
+        cudaFuncAttributes fa;
+        if (cudaFuncGetAttributes(&fa, attn_kernel) != cudaSuccess || fa.numRegs != kRegsLaunch)
+            return DSA_ERR_CUDA;
         if (cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kAttnSmem) != cudaSuccess)
             return DSA_ERR_CUDA;
-        attr_set = true;
+        checked = true;
     }
     CUtensorMap tm_q, tm_out;
     if (!make_tmap_bf16(&tm_q, q, kD, static_cast<uint64_t>(chunk) * kH, kD * 2, 64, 64))
