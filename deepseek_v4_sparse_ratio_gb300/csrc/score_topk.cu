@@ -41,7 +41,8 @@ namespace {
 
 constexpr int kTok = 8;            // query rows per work unit
 constexpr int kStages = 2;         // key-block ring depth
-constexpr int kScoreThreads = 320; // warp 0 TMA, warp 1 MMA, warps 2-9 epilogue
+constexpr int kEpiWarps = 16;      // one 4-row x 32-lane slice of a TMEM half each
+constexpr int kScoreThreads = 32 * (2 + kEpiWarps);  // warp 0 TMA, warp 1 MMA, 2-17 epilogue
 constexpr uint32_t kBBytes = 2 * 2 * 256 * 128;  // [half][k-chunk][256 rows][128 B]
 constexpr uint32_t kAStage = 2 * 128 * 128;      // [k-chunk][128 rows][128 B]
 constexpr uint32_t kOffB = 0;
@@ -129,7 +130,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         mbar_init(b_empty, 1);
         for (int h = 0; h < 2; ++h) {
             mbar_init(&t_full[h], 1);
-            mbar_init(&t_empty[h], 8);
+            mbar_init(&t_empty[h], kEpiWarps);
         }
         mbar_init(drain, 1);
         *abort_flag = 0;
@@ -226,22 +227,24 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         mma_commit(drain);
         drain_wait(drain, 0);
     } else if (warp >= 2) {
-        // ---------------- epilogue: 8 warps; TMEM sub-partition = warp % 4
+        // ---------------- epilogue: 16 warps; warp reads TMEM sub-partition sp = warp % 4
+        // (pooled rows j = 32sp .. 32sp+31 of the block) for token tl of each 4-token half
         const int ew = warp - 2;
         const int sp = warp & 3;
-        const int cg = ew >> 2;  // tokens {2cg, 2cg+1} of each 4-token half
+        const int tl = ew >> 2;
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(sp * 32) << 16);
+        const int nthr = 32 * kEpiWarps;
         int tu0 = 0, tu1 = 0;
         // Every epilogue warp walks every unit so that the named barriers
-        // below always see all 256 threads, even after an abort.
+        // below always see all epilogue threads, even after an abort.
         for (int u = blockIdx.x; u < p.n_units; u += gridDim.x) {
             const Unit x = unit_geom(p, u);
-            asm volatile("bar.sync 1, 256;" ::: "memory");
-            for (int i = ew * 32 + lane; i < kTok * kHI; i += 256) {
+            asm volatile("bar.sync 1, %0;" ::"r"(nthr) : "memory");
+            for (int i = ew * 32 + lane; i < kTok * kHI; i += nthr) {
                 const int row = x.row0 + i / kHI;
                 sW[i] = row < p.R ? __ldg(&p.w[(p.r0 + row) * kHI + (i % kHI)]) : 0.0f;
             }
-            asm volatile("bar.sync 1, 256;" ::: "memory");
+            asm volatile("bar.sync 1, %0;" ::"r"(nthr) : "memory");
             bool ok = !*abort_flag;
             for (int kb = x.b0; kb < x.b1 && ok; ++kb) {
                 const int64_t j = static_cast<int64_t>(kb) * kScoreBlock + sp * 32 + lane;
@@ -254,43 +257,47 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                         }
                         tc_fence_after();
                         ++tu;
-#pragma unroll 1
-                        for (int tt = 0; tt < 2; ++tt) {
-                            const int tl = cg * 2 + tt;
-                            const int ti = half * 4 + tl;
-                            uint32_t va[32], vb[32];
-                            const uint32_t col = half * 256 + tl * 64;
-                            tmem_ld32(lane_addr + col, va);
-                            tmem_ld32(lane_addr + col + 32, vb);
+                        const int ti = half * 4 + tl;
+                        // sum_h w_h * ReLU(v_h): even heads in .x, odd heads in .y of a
+                        // packed pair, added at the end (a fixed order for every tile)
+                        const float4 *w4 = reinterpret_cast<const float4 *>(sW + ti * kHI);
+                        const uint32_t col = half * 256 + tl * 64;
+                        uint64_t acc = 0;
+#pragma unroll
+                        for (int hp = 0; hp < 2; ++hp) {
+                            uint32_t v[32];
+                            tmem_ld32(lane_addr + col + 32 * hp, v);
                             tmem_wait_ld();
-                            const float4 *w4 = reinterpret_cast<const float4 *>(sW + ti * kHI);
-                            float acc = 0.0f;
-#pragma unroll
-                            for (int q = 0; q < 8; ++q) {
-                                const float4 ww = w4[q];
-                                acc = fmaf(ww.x, fmaxf(__uint_as_float(va[4 * q + 0]), 0.0f), acc);
-                                acc = fmaf(ww.y, fmaxf(__uint_as_float(va[4 * q + 1]), 0.0f), acc);
-                                acc = fmaf(ww.z, fmaxf(__uint_as_float(va[4 * q + 2]), 0.0f), acc);
-                                acc = fmaf(ww.w, fmaxf(__uint_as_float(va[4 * q + 3]), 0.0f), acc);
+                            if (hp == 1) {
+                                tc_fence_before();
+                                __syncwarp();
+                                if (lane == 0) mbar_arrive(&t_empty[half]);
                             }
 #pragma unroll
                             for (int q = 0; q < 8; ++q) {
-                                const float4 ww = w4[8 + q];
-                                acc = fmaf(ww.x, fmaxf(__uint_as_float(vb[4 * q + 0]), 0.0f), acc);
-                                acc = fmaf(ww.y, fmaxf(__uint_as_float(vb[4 * q + 1]), 0.0f), acc);
-                                acc = fmaf(ww.z, fmaxf(__uint_as_float(vb[4 * q + 2]), 0.0f), acc);
-                                acc = fmaf(ww.w, fmaxf(__uint_as_float(vb[4 * q + 3]), 0.0f), acc);
+                                const float4 ww = w4[8 * hp + q];
+                                uint64_t w01, w23, r01, r23;
+                                asm("mov.b64 %0, {%1, %2};" : "=l"(w01) : "f"(ww.x), "f"(ww.y));
+                                asm("mov.b64 %0, {%1, %2};" : "=l"(w23) : "f"(ww.z), "f"(ww.w));
+                                asm("mov.b64 %0, {%1, %2};"
+                                    : "=l"(r01)
+                                    : "f"(fmaxf(__uint_as_float(v[4 * q]), 0.0f)),
+                                      "f"(fmaxf(__uint_as_float(v[4 * q + 1]), 0.0f)));
+                                asm("mov.b64 %0, {%1, %2};"
+                                    : "=l"(r23)
+                                    : "f"(fmaxf(__uint_as_float(v[4 * q + 2]), 0.0f)),
+                                      "f"(fmaxf(__uint_as_float(v[4 * q + 3]), 0.0f)));
+                                asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(w01), "l"(r01));
+                                asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(acc) : "l"(w23), "l"(r23));
                             }
-                            store_score(p, x.row0 + ti, j, acc);
                         }
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0) mbar_arrive(&t_empty[half]);
+                        float ae, ao;
+                        asm("mov.b64 {%0, %1}, %2;" : "=f"(ae), "=f"(ao) : "l"(acc));
+                        store_score(p, x.row0 + ti, j, ae + ao);
                     }
                 } else {
                     for (int half = 0; half < 2; ++half)
-                        for (int tt = 0; tt < 2; ++tt)
-                            store_score(p, x.row0 + half * 4 + cg * 2 + tt, j, -INFINITY);
+                        store_score(p, x.row0 + half * 4 + tl, j, -INFINITY);
                 }
             }
         }
@@ -305,11 +312,10 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 
 // ------------------------------------------------------------------ top-k kernel
 
-constexpr int kTopkThreads = 512;
+constexpr int kTopkThreads = 256;
 constexpr int kTopkWarps = kTopkThreads / 32;
-constexpr int kStageMaxFloats = 49152;  // rows up to this long are staged in shared memory
 constexpr int kBins = 2048;
-constexpr int kCandCap = 4096;
+constexpr int kCandCap = 2048;
 
 __device__ __forceinline__ uint32_t order_key(float f) {
     const uint32_t b = __float_as_uint(f);
@@ -397,13 +403,14 @@ __device__ __forceinline__ void radix_select(KeyAt key_at, int64_t count, uint32
     *need_out = need;
 }
 
-template <bool kStaged>
+// One CTA per query row; every pass walks the row in per-warp contiguous
+// segments (coalesced, and the last pass must emit in index order).
 __global__ void __launch_bounds__(kTopkThreads)
     topk_kernel(const float *__restrict__ scores, int64_t stride, int64_t n, int64_t offset,
                 int64_t r0, int32_t k, int32_t *__restrict__ sel) {
-    extern __shared__ float srow[];
     __shared__ uint32_t hist[kBins];
     __shared__ uint32_t cand[kCandCap];
+    __shared__ int32_t cand_j[kCandCap];
     __shared__ uint32_t warp_sums[kTopkWarps + 1];
     __shared__ uint32_t s_bin, s_above, s_cnt;
     __shared__ float s_min[kTopkWarps], s_max[kTopkWarps];
@@ -419,18 +426,12 @@ __global__ void __launch_bounds__(kTopkThreads)
         return;
     }
     const float *src = scores + static_cast<int64_t>(row) * stride;
-    if (kStaged) {
-        const float4 *s4 = reinterpret_cast<const float4 *>(src);
-        float4 *d4 = reinterpret_cast<float4 *>(srow);
-        for (int64_t i = threadIdx.x; i < L / 4; i += kTopkThreads) d4[i] = __ldcs(&s4[i]);
-        for (int64_t i = (L / 4) * 4 + threadIdx.x; i < L; i += kTopkThreads) srow[i] = src[i];
-        __syncthreads();
-        src = srow;
-    }
+    const int64_t seg = ((L + kTopkWarps - 1) / kTopkWarps + 31) / 32 * 32;
+    const int64_t lo = min(L, seg * warp), hi = min(L, seg * (warp + 1));
 
     // ---- 1. range of the row
     float vmin = INFINITY, vmax = -INFINITY;
-    for (int64_t j = threadIdx.x; j < L; j += kTopkThreads) {
+    for (int64_t j = lo + lane; j < hi; j += 32) {
         const float v = src[j];
         vmin = fminf(vmin, v);
         vmax = fmaxf(vmax, v);
@@ -456,6 +457,7 @@ __global__ void __launch_bounds__(kTopkThreads)
     }
 
     uint32_t thr, need_eq;
+    bool counted = false;  // w_gt / w_eq already hold the per-segment counts
     if (vmin == vmax) {
         // every visible score is equal: the k lowest indices
         thr = order_key(vmax);
@@ -465,45 +467,66 @@ __global__ void __launch_bounds__(kTopkThreads)
         // of a higher bin is >= every element of a lower bin
         const float scale = static_cast<float>(kBins) / (vmax - vmin);
         auto bin_of = [&](float v) { return min(kBins - 1, static_cast<int>((v - vmin) * scale)); };
-        for (int64_t j = threadIdx.x; j < L; j += kTopkThreads) atomicAdd(&hist[bin_of(src[j])], 1u);
+        for (int64_t j = lo + lane; j < hi; j += 32) atomicAdd(&hist[bin_of(src[j])], 1u);
         __syncthreads();
         find_bin(hist, kBins, static_cast<uint32_t>(k), warp_sums, &s_bin, &s_above);
         const int bstar = static_cast<int>(s_bin);
         const uint32_t need = static_cast<uint32_t>(k) - s_above;
-        // ---- 3. exact selection among the threshold bin's elements
-        for (int64_t j = threadIdx.x; j < L; j += kTopkThreads) {
+        // ---- 3. the threshold bin's elements are the candidates; count each
+        // segment's elements above that bin on the way
+        uint32_t above = 0;
+        for (int64_t j = lo + lane; j < hi; j += 32) {
             const float v = src[j];
-            if (bin_of(v) == bstar) {
+            const int b = bin_of(v);
+            above += b > bstar;
+            if (b == bstar) {
                 const uint32_t c = atomicAdd(&s_cnt, 1u);
-                if (c < kCandCap) cand[c] = order_key(v);
+                if (c < kCandCap) {
+                    cand[c] = order_key(v);
+                    cand_j[c] = static_cast<int32_t>(j);
+                }
             }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) above += __shfl_xor_sync(0xFFFFFFFFu, above, o);
+        if (lane == 0) {
+            w_gt[warp] = above;
+            w_eq[warp] = 0;
         }
         __syncthreads();
         const uint32_t cnt = s_cnt;
         if (cnt <= kCandCap) {
-            radix_select([&](int64_t j) { return cand[j]; }, cnt, need, hist, warp_sums, &s_bin,
+            radix_select([&](int64_t c) { return cand[c]; }, cnt, need, hist, warp_sums, &s_bin,
                          &s_above, &thr, &need_eq);
+            // candidates above / equal to the threshold, by segment
+            for (uint32_t c = threadIdx.x; c < cnt; c += kTopkThreads) {
+                const int w = static_cast<int>(cand_j[c] / seg);
+                if (cand[c] > thr) atomicAdd(&w_gt[w], 1u);
+                else if (cand[c] == thr) atomicAdd(&w_eq[w], 1u);
+            }
+            __syncthreads();
+            counted = true;
         } else {
             radix_select([&](int64_t j) { return order_key(src[j]); }, L, static_cast<uint32_t>(k),
                          hist, warp_sums, &s_bin, &s_above, &thr, &need_eq);
         }
     }
 
-    // ---- 4. emit kept indices ascending: each warp owns a contiguous segment
-    const int64_t seg = ((L + kTopkWarps - 1) / kTopkWarps + 31) / 32 * 32;
-    const int64_t lo = min(L, seg * warp), hi = min(L, seg * (warp + 1));
-    uint32_t ngt = 0, neq = 0;
-    for (int64_t base = lo; base < hi; base += 32) {
-        const int64_t j = base + lane;
-        const uint32_t u = j < hi ? order_key(src[j]) : 0u;
-        ngt += __popc(__ballot_sync(0xFFFFFFFFu, j < hi && u > thr));
-        neq += __popc(__ballot_sync(0xFFFFFFFFu, j < hi && u == thr));
+    // ---- 4. emit kept indices ascending: each warp owns its contiguous segment
+    if (!counted) {
+        uint32_t ngt = 0, neq = 0;
+        for (int64_t base = lo; base < hi; base += 32) {
+            const int64_t j = base + lane;
+            const uint32_t u = j < hi ? order_key(src[j]) : 0u;
+            ngt += __popc(__ballot_sync(0xFFFFFFFFu, j < hi && u > thr));
+            neq += __popc(__ballot_sync(0xFFFFFFFFu, j < hi && u == thr));
+        }
+        if (lane == 0) {
+            w_gt[warp] = ngt;
+            w_eq[warp] = neq;
+        }
+        __syncthreads();
     }
-    if (lane == 0) {
-        w_gt[warp] = ngt;
-        w_eq[warp] = neq;
-    }
-    __syncthreads();
     uint32_t base_gt = 0, base_eq = 0;
     for (int w = 0; w < warp; ++w) {
         base_gt += w_gt[w];
@@ -593,22 +616,8 @@ int launch_score_tile(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const fl
 int launch_topk_tile(const float *scores, int64_t stride, int64_t n, int64_t offset, int64_t r0,
                      int64_t R, int32_t k, int32_t *sel, int32_t *status, cudaStream_t s) {
     (void)status;
-    const int64_t Lmax = std::min<int64_t>(n, (offset + r0 + R) / kRatio);
-    if (Lmax <= kStageMaxFloats) {
-        const size_t bytes = static_cast<size_t>(std::max<int64_t>(Lmax, 4)) * sizeof(float);
-        static bool attr_set = false;
-        if (!attr_set) {
-            if (cudaFuncSetAttribute(topk_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     kStageMaxFloats * 4) != cudaSuccess)
-                return DSA_ERR_CUDA;
-            attr_set = true;
-        }
-        topk_kernel<true><<<static_cast<unsigned>(R), kTopkThreads, bytes, s>>>(scores, stride, n,
-                                                                               offset, r0, k, sel);
-    } else {
-        topk_kernel<false><<<static_cast<unsigned>(R), kTopkThreads, 0, s>>>(scores, stride, n,
-                                                                            offset, r0, k, sel);
-    }
+    topk_kernel<<<static_cast<unsigned>(R), kTopkThreads, 0, s>>>(scores, stride, n, offset, r0, k,
+                                                                 sel);
     return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
