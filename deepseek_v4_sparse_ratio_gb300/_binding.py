@@ -22,7 +22,9 @@ DSA_ERR_DIVERGED, DSA_ERR_SCRATCH, DSA_ERR_CUDA, DSA_ERR_TIMEOUT = -5, -6, -7, -
 DSA_ERR_BOUNDS, DSA_ERR_RAW_RANGE = -9, -10
 
 EXPORTS = ("dsa_pool_append", "dsa_score_scratch_bytes", "dsa_index_score_topk",
-           "dsa_window_sparse_attn", "dsa_prefill_chunk", "dsa_strerror")
+           "dsa_window_sparse_attn", "dsa_prefill_chunk", "dsa_strerror",
+           "dsa_index_score_topk_noalloc")
+DSA_STATIC_SCRATCH_BYTES = 16 << 20
 
 
 class DsaError(RuntimeError):
@@ -59,10 +61,11 @@ def load(path: str | None = None):
                                            ctypes.c_float, P, P, P]
     lib.dsa_prefill_chunk.argtypes = [S, P, i64, i64, P, P, P, P, i64, i64, i32, i32,
                                       ctypes.c_float, i64, P, sz, P, P, P, P]
+    lib.dsa_index_score_topk_noalloc.argtypes = [P, P, P, i64, i64, i64, i32, i32, i64, P, P, P]
     lib.dsa_strerror.argtypes = [ctypes.c_int]
     lib.dsa_strerror.restype = ctypes.c_char_p
     for f in ("dsa_pool_append", "dsa_index_score_topk", "dsa_window_sparse_attn",
-              "dsa_prefill_chunk"):
+              "dsa_prefill_chunk", "dsa_index_score_topk_noalloc"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -164,6 +167,16 @@ def dsa_index_score_topk(q_idx, w, pooled_ik, n_pooled: int, chunk: int, offset:
                                      ratio, index_topk, tile_rows, _p(scratch), _nbytes(scratch),
                                      _p(sel), _p(dev_status), _s(stream))
     _check(rc, "dsa_index_score_topk")
+
+
+def dsa_index_score_topk_noalloc(q_idx, w, pooled_ik, n_pooled: int, chunk: int, offset: int,
+                                 ratio: int, index_topk: int, tile_rows: int, sel,
+                                 dev_status=None, stream=None) -> None:
+    """dsa_index_score_topk with the library's own score scratch (no allocation)."""
+    rc = load().dsa_index_score_topk_noalloc(_p(q_idx), _p(w), _p(pooled_ik), n_pooled, chunk,
+                                             offset, ratio, index_topk, tile_rows, _p(sel),
+                                             _p(dev_status), _s(stream))
+    _check(rc, "dsa_index_score_topk_noalloc")
 
 
 def dsa_window_sparse_attn(q, raw_kv, raw_start: int, pooled_kv, n_pooled: int, sel,

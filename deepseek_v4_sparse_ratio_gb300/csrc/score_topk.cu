@@ -30,6 +30,7 @@
 #include <math.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -679,6 +680,59 @@ extern "C" int dsa_index_score_topk(const void *q_idx, const float *w, const voi
     int rc = check_score_topk(q_idx, w, pooled_ik, n_pooled, chunk, offset, ratio, index_topk,
                               tile_rows, scratch, scratch_bytes, sel);
     if (rc != DSA_OK) return rc;
+    return run_score_topk(q_idx, w, pooled_ik, n_pooled, chunk, offset, index_topk, tile_rows,
+                          scratch, sel, dev_status, static_cast<cudaStream_t>(stream));
+}
+
+// ------------------------------------------------------------------ no-allocation variant
+//
+// Score scratch held by the library itself, for callers that cannot hand it
+// device memory. Every device that loads the library keeps this array until
+// the process exits; all calls on a device share it.
+namespace dsa {
+namespace {
+
+__device__ __align__(256) static float g_static_scratch[DSA_STATIC_SCRATCH_BYTES / sizeof(float)];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+void *g_static_ptr[kMaxDevices] = {};
+
+// Device address of g_static_scratch on the current device, looked up once per
+// device (the host-side name of the array is not a device address).
+int static_scratch(void **out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DSA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_static_mu);
+    if (!g_static_ptr[dev]) {
+        void *ptr = nullptr;
+        if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || !ptr)
+            return DSA_ERR_CUDA;
+        g_static_ptr[dev] = ptr;
+    }
+    *out = g_static_ptr[dev];
+    return DSA_OK;
+}
+
+}  // namespace
+}  // namespace dsa
+
+extern "C" int dsa_index_score_topk_noalloc(const void *q_idx, const float *w,
+                                            const void *pooled_ik, int64_t n_pooled,
+                                            int64_t chunk, int64_t offset, int32_t ratio,
+                                            int32_t index_topk, int64_t tile_rows, int32_t *sel,
+                                            int32_t *dev_status, void *stream) {
+    using namespace dsa;
+    // validate with the library-held scratch standing in for the caller's buffer
+    const void *probe = reinterpret_cast<const void *>(uintptr_t{256});
+    int rc = check_score_topk(q_idx, w, pooled_ik, n_pooled, chunk, offset, ratio, index_topk,
+                              tile_rows, probe, DSA_STATIC_SCRATCH_BYTES, sel);
+    if (rc != DSA_OK) return rc;
+    void *scratch = nullptr;
+    if (n_pooled > index_topk) {
+        rc = static_scratch(&scratch);
+        if (rc != DSA_OK) return rc;
+    }
     return run_score_topk(q_idx, w, pooled_ik, n_pooled, chunk, offset, index_topk, tile_rows,
                           scratch, sel, dev_status, static_cast<cudaStream_t>(stream));
 }

@@ -209,6 +209,43 @@ int dsa_prefill_chunk(dsa_pool_state *st, const void *raw_kv, int64_t raw_start,
                       void *scratch, size_t scratch_bytes, int32_t *sel, void *out,
                       int32_t *dev_status, void *stream);
 
+/*
+ * Library-held score scratch: the size of the device array that
+ * dsa_index_score_topk_noalloc uses instead of a caller buffer (16 MiB, one
+ * per device that loads the library, kept until the process exits).
+ */
+#define DSA_STATIC_SCRATCH_BYTES ((size_t)16 << 20)
+
+/*
+ * (b)+(c) as dsa_index_score_topk, for callers that cannot allocate device
+ * memory when they call in -- for example code that only receives tensor
+ * pointers from a host framework's execution loop, or a process that fixes its
+ * device-memory budget at start-up and must not allocate while serving. The
+ * score scratch is a file-scope device array inside libdsa.so
+ * (DSA_STATIC_SCRATCH_BYTES); this call allocates nothing and frees nothing.
+ * The pages have no counterpart to this entry point: it is an addition of this
+ * library.
+ *
+ *   Arguments, paths and results are those of dsa_index_score_topk without
+ *   `scratch` / `scratch_bytes`. On the full path the tile must fit the array:
+ *   dsa_score_scratch_bytes(min(tile_rows, chunk), n_pooled) <= DSA_STATIC_SCRATCH_BYTES,
+ *   otherwise DSA_ERR_SCRATCH is returned and nothing is enqueued (pick a
+ *   smaller tile_rows; the selection does not depend on it).
+ *   The first full-path call on a device looks up the array's device address
+ *   (cudaGetSymbolAddress) on the current device; make that first call before
+ *   any stream capture.
+ *   All calls on a device share the one array and it keeps the last call's
+ *   contents (nothing in it needs to start at zero). Calls whose work overlaps
+ *   on the GPU -- on different streams, or from several threads -- race on it;
+ *   serialize them.
+ * Errors: as dsa_index_score_topk; DSA_ERR_SCRATCH for a tile beyond the array;
+ * DSA_ERR_CUDA if the array's address cannot be obtained.
+ */
+int dsa_index_score_topk_noalloc(const void *q_idx, const float *w, const void *pooled_ik,
+                                 int64_t n_pooled, int64_t chunk, int64_t offset, int32_t ratio,
+                                 int32_t index_topk, int64_t tile_rows, int32_t *sel,
+                                 int32_t *dev_status, void *stream);
+
 /* Static description of a DSA_* status code. */
 const char *dsa_strerror(int code);
 
