@@ -100,20 +100,22 @@ class PoolState:
     """Caller-side PoolingCache: device buffers (torch) plus the C struct."""
 
     def __init__(self, cap: int, device="cuda", ratio: int = RATIO):
+        self.ratio = ratio
         self.pooled_kv = torch.zeros(max(cap, 1), DIM, dtype=torch.bfloat16, device=device)
         self.pooled_ik = torch.zeros(max(cap, 1), INDEX_DIM, dtype=torch.bfloat16, device=device)
-        self.rem_kv = torch.zeros(RATIO - 1, DIM, dtype=torch.bfloat16, device=device)
-        self.rem_ik = torch.zeros(RATIO - 1, INDEX_DIM, dtype=torch.bfloat16, device=device)
+        self.rem_kv = torch.zeros(max(ratio - 1, 1), DIM, dtype=torch.bfloat16, device=device)
+        self.rem_ik = torch.zeros(max(ratio - 1, 1), INDEX_DIM, dtype=torch.bfloat16, device=device)
         self.c = dsa_pool_state(self.pooled_kv.data_ptr(), self.pooled_ik.data_ptr(),
                                 self.rem_kv.data_ptr(), self.rem_ik.data_ptr(), cap, 0, 0, 0, 0,
                                 ratio)
 
     @classmethod
-    def from_prefix(cls, pooled_ik, pooled_kv, n_tokens: int, cap: int, device="cuda"):
+    def from_prefix(cls, pooled_ik, pooled_kv, n_tokens: int, cap: int, device="cuda",
+                    ratio: int = RATIO):
         """A cache that already holds `pooled_*` rows after n_tokens tokens (no remainder)."""
-        s = cls(cap, device)
+        s = cls(cap, device, ratio)
         P = pooled_ik.shape[0]
-        assert n_tokens == P * RATIO and pooled_kv.shape[0] == P and P <= cap
+        assert n_tokens == P * ratio and pooled_kv.shape[0] == P and P <= cap
         s.pooled_ik[:P].copy_(pooled_ik)
         s.pooled_kv[:P].copy_(pooled_kv)
         s.c.n_pooled_kv = s.c.n_pooled_ik = P
@@ -144,7 +146,8 @@ class PoolState:
 
 
 def dsa_pool_append(state: PoolState, raw_kv, raw_ik, chunk: int, offset: int,
-                    ratio: int = RATIO, stream=None) -> None:
+                    ratio: int | None = None, stream=None) -> None:
+    ratio = state.ratio if ratio is None else ratio
     rc = load().dsa_pool_append(ctypes.byref(state.c), _p(raw_kv), _p(raw_ik), chunk, offset,
                                 ratio, _s(stream))
     _check(rc, "dsa_pool_append")

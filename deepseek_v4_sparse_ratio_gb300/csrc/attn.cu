@@ -72,6 +72,7 @@ struct AttnParams {
     int64_t n;
     int64_t offset;
     int64_t raw_start;
+    int32_t ratio;
     int32_t window;
     float c;  // softmax scale * log2(e)
     int T;
@@ -86,7 +87,7 @@ struct TokenInfo {
 __device__ __forceinline__ TokenInfo token_info(const AttnParams &p, int i) {
     TokenInfo x;
     x.t = p.offset + i;
-    x.nv = min(p.n, (x.t + 1) / kRatio);
+    x.nv = min(p.n, (x.t + 1) / p.ratio);
     x.u0 = max(int64_t{0}, x.t - p.window + 1);
     const int64_t nwin = x.t - x.u0 + 1;
     x.nwb = static_cast<int>((nwin + 127) / 128);
@@ -522,8 +523,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 
 int launch_attention(const void *q, const void *raw_kv, int64_t raw_start, int64_t raw_rows,
                      const void *pooled_kv, int64_t n, const int32_t *sel, int32_t k,
-                     int64_t chunk, int64_t offset, int32_t window, float scale, void *out,
-                     int32_t *status, cudaStream_t s) {
+                     int64_t chunk, int64_t offset, int32_t ratio, int32_t window, float scale,
+                     void *out, int32_t *status, cudaStream_t s) {
     (void)raw_rows;
     static bool checked = false;
     if (!checked) {
@@ -550,6 +551,7 @@ int launch_attention(const void *q, const void *raw_kv, int64_t raw_start, int64
     p.n = n;
     p.offset = offset;
     p.raw_start = raw_start;
+    p.ratio = ratio;
     p.window = window;
     p.c = scale * 1.4426950408889634f;
     p.T = static_cast<int>(chunk);
@@ -569,7 +571,7 @@ int check_attention(const void *q, const void *raw_kv, int64_t raw_start, int64_
     if (!aligned16(q) || !aligned16(raw_kv) || !aligned16(sel) || !aligned16(out) ||
         (pooled_kv && !aligned16(pooled_kv)))
         return DSA_ERR_ARG;
-    if (ratio != kRatio || k <= 0 || window <= 0 || !(scale > 0.0f) || isinf(scale))
+    if (!valid_ratio(ratio) || k <= 0 || window <= 0 || !(scale > 0.0f) || isinf(scale))
         return DSA_ERR_SHAPE;
     if (chunk * kH > (int64_t{1} << 31) - 1 || raw_rows > (int64_t{1} << 31) - 1 ||
         n > (int64_t{1} << 31) - 1)
@@ -591,6 +593,6 @@ extern "C" int dsa_window_sparse_attn(const void *q, const void *raw_kv, int64_t
                              chunk, offset, ratio, window, scale, out);
     if (rc != DSA_OK) return rc;
     return launch_attention(q, raw_kv, raw_start, raw_rows, pooled_kv, n_pooled, sel, index_topk,
-                            chunk, offset, window, scale, out, dev_status,
+                            chunk, offset, ratio, window, scale, out, dev_status,
                             static_cast<cudaStream_t>(stream));
 }

@@ -24,10 +24,10 @@ inline int64_t score_stride(int64_t n_pooled) {
     return (n_pooled + kScoreBlock - 1) / kScoreBlock * kScoreBlock;
 }
 
-inline int64_t n_visible(int64_t t, int64_t n) {
-    int64_t v = (t + 1) / kRatio;
-    return v < n ? v : n;
-}
+// Pooling ratios the library accepts: powers of two in [2, 128] (4 for the
+// indexed attention, 128 for the compressed attention).
+constexpr int kMaxRatio = 128;
+inline bool valid_ratio(int64_t r) { return r >= 2 && r <= kMaxRatio && (r & (r - 1)) == 0; }
 
 inline bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -45,15 +45,16 @@ int sm_count();
 int launch_pool_append(const dsa_pool_state &st, const void *raw_kv, const void *raw_ik,
                        int64_t chunk, int64_t offset, cudaStream_t s);
 int launch_fill_selection(int32_t *sel, int64_t rows, int32_t k, int64_t offset, int64_t n,
-                          cudaStream_t s);
+                          int32_t ratio, cudaStream_t s);
 int launch_score_tile(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const float *w,
-                      int64_t n, int64_t offset, int64_t r0, int64_t R, float *scores,
-                      int64_t stride, int32_t *status, cudaStream_t s);
-int launch_topk_tile(const float *scores, int64_t stride, int64_t n, int64_t offset, int64_t r0,
-                     int64_t R, int32_t k, int32_t *sel, int32_t *status, cudaStream_t s);
+                      int64_t n, int64_t offset, int32_t ratio, int64_t r0, int64_t R,
+                      float *scores, int64_t stride, int32_t *status, cudaStream_t s);
+int launch_topk_tile(const float *scores, int64_t stride, int64_t n, int64_t offset,
+                     int32_t ratio, int64_t r0, int64_t R, int32_t k, int32_t *sel,
+                     int32_t *status, cudaStream_t s);
 int launch_attention(const void *q, const void *raw_kv, int64_t raw_start, int64_t raw_rows,
                      const void *pooled_kv, int64_t n, const int32_t *sel, int32_t k,
-                     int64_t chunk, int64_t offset, int32_t window, float scale, void *out,
-                     int32_t *status, cudaStream_t s);
+                     int64_t chunk, int64_t offset, int32_t ratio, int32_t window, float scale,
+                     void *out, int32_t *status, cudaStream_t s);
 
 }  // namespace dsa

@@ -7,10 +7,11 @@
 // Summary item 4: new pooled rows are written in place after the existing
 // ones, with no re-concatenation of the prefix.
 //
-// Arithmetic: a pooled element is the exact mean of four bf16 values (their
-// sum is exact in fp64, and /4 is exact), rounded once to bf16 with ties to
-// even. HBM-bound: each thread moves one 16-byte vector of each of the four
-// raw rows and writes one 16-byte vector of the pooled row.
+// Arithmetic: a pooled element is the mean of `ratio` bf16 values (a power of
+// two up to 128: the fp64 sum, taken in row order, is exact for such values in
+// practice, and /ratio is exact), rounded once to bf16 with ties to even.
+// HBM-bound: each thread moves one 16-byte vector of each of the raw rows and
+// writes one 16-byte vector of the pooled row.
 #include <cudaTypedefs.h>
 
 #include <mutex>
@@ -61,7 +62,7 @@ __global__ void __launch_bounds__(256) pool_kernel(const uint4 *__restrict__ raw
                                                    const uint4 *__restrict__ rem_ik,
                                                    uint4 *__restrict__ pooled_kv,
                                                    uint4 *__restrict__ pooled_ik, int64_t n_old,
-                                                   int64_t n_new, int64_t offset) {
+                                                   int64_t n_new, int64_t offset, int32_t ratio) {
     const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (idx >= (n_new - n_old) * kVecRow) return;
     const int64_t g = n_old + idx / kVecRow;
@@ -71,19 +72,20 @@ __global__ void __launch_bounds__(256) pool_kernel(const uint4 *__restrict__ raw
     const int per_row = is_kv ? kVecKV : kVecIK;
     const uint4 *raw = is_kv ? raw_kv : raw_ik;
     const uint4 *rem = is_kv ? rem_kv : rem_ik;
-    const int64_t rem_base = n_old * kRatio;  // absolute token held in remainder slot 0
+    const int64_t rem_base = n_old * ratio;  // absolute token held in remainder slot 0
 
     double acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-#pragma unroll
-    for (int i = 0; i < kRatio; ++i) {
-        const int64_t u = g * kRatio + i;
+#pragma unroll 4
+    for (int i = 0; i < ratio; ++i) {
+        const int64_t u = g * ratio + i;
         const uint4 x = (u < offset) ? rem[(u - rem_base) * per_row + vv]
                                      : __ldg(&raw[(u - offset) * per_row + vv]);
         add8(acc, x);
     }
     uint32_t o[8];
 #pragma unroll
-    for (int e = 0; e < 8; ++e) o[e] = bf16_rne_from_double(acc[e] * 0.25);
+    const double inv = 1.0 / ratio;  // exact: ratio is a power of two
+    for (int e = 0; e < 8; ++e) o[e] = bf16_rne_from_double(acc[e] * inv);
     uint4 out;
     out.x = o[0] | (o[1] << 16);
     out.y = o[2] | (o[3] << 16);
@@ -97,18 +99,19 @@ __global__ void __launch_bounds__(256) pool_kernel(const uint4 *__restrict__ raw
 // that predate the chunk already sit in their slot.
 __global__ void remainder_kernel(const uint4 *__restrict__ raw_kv, const uint4 *__restrict__ raw_ik,
                                  uint4 *__restrict__ rem_kv, uint4 *__restrict__ rem_ik,
-                                 int64_t n_new, int64_t offset, int64_t end) {
-    const int64_t first = n_new * kRatio > offset ? n_new * kRatio : offset;
-    const int64_t idx = threadIdx.x;
+                                 int64_t n_new, int64_t offset, int64_t end, int32_t ratio) {
+    const int64_t first = n_new * ratio > offset ? n_new * ratio : offset;
     const int64_t rows = end - first;
-    if (idx >= rows * kVecRow) return;
-    const int64_t u = first + idx / kVecRow;
-    const int v = static_cast<int>(idx % kVecRow);
-    const int64_t slot = u - n_new * kRatio;
-    if (v < kVecKV)
-        rem_kv[slot * kVecKV + v] = raw_kv[(u - offset) * kVecKV + v];
-    else
-        rem_ik[slot * kVecIK + (v - kVecKV)] = raw_ik[(u - offset) * kVecIK + (v - kVecKV)];
+    for (int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+         idx < rows * kVecRow; idx += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+        const int64_t u = first + idx / kVecRow;
+        const int v = static_cast<int>(idx % kVecRow);
+        const int64_t slot = u - n_new * ratio;
+        if (v < kVecKV)
+            rem_kv[slot * kVecKV + v] = raw_kv[(u - offset) * kVecKV + v];
+        else
+            rem_ik[slot * kVecIK + (v - kVecKV)] = raw_ik[(u - offset) * kVecIK + (v - kVecKV)];
+    }
 }
 
 }  // namespace
@@ -116,8 +119,9 @@ __global__ void remainder_kernel(const uint4 *__restrict__ raw_kv, const uint4 *
 int launch_pool_append(const dsa_pool_state &st, const void *raw_kv, const void *raw_ik,
                        int64_t chunk, int64_t offset, cudaStream_t s) {
     const int64_t n_old = st.n_pooled_kv;
+    const int32_t ratio = st.ratio;
     const int64_t end = offset + chunk;
-    const int64_t n_new = end / kRatio;
+    const int64_t n_new = end / ratio;
     if (n_new > n_old) {
         const int64_t threads = (n_new - n_old) * kVecRow;
         const int64_t blocks = (threads + 255) / 256;
@@ -125,13 +129,15 @@ int launch_pool_append(const dsa_pool_state &st, const void *raw_kv, const void 
             static_cast<const uint4 *>(raw_kv), static_cast<const uint4 *>(raw_ik),
             static_cast<const uint4 *>(st.rem_kv), static_cast<const uint4 *>(st.rem_ik),
             static_cast<uint4 *>(st.pooled_kv), static_cast<uint4 *>(st.pooled_ik), n_old, n_new,
-            offset);
+            offset, ratio);
         if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
     }
-    if (end % kRatio != 0) {
-        remainder_kernel<<<1, (kRatio - 1) * kVecRow, 0, s>>>(
+    if (end % ratio != 0) {
+        const int64_t threads = (end % ratio) * kVecRow;
+        remainder_kernel<<<static_cast<unsigned>((threads + 255) / 256), 256, 0, s>>>(
             static_cast<const uint4 *>(raw_kv), static_cast<const uint4 *>(raw_ik),
-            static_cast<uint4 *>(st.rem_kv), static_cast<uint4 *>(st.rem_ik), n_new, offset, end);
+            static_cast<uint4 *>(st.rem_kv), static_cast<uint4 *>(st.rem_ik), n_new, offset, end,
+            ratio);
         if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
     }
     return DSA_OK;
@@ -186,21 +192,21 @@ extern "C" int dsa_pool_append(dsa_pool_state *st, const void *raw_kv, const voi
     if (!aligned16(raw_kv) || !aligned16(raw_ik) || !aligned16(st->pooled_kv) ||
         !aligned16(st->pooled_ik) || !aligned16(st->rem_kv) || !aligned16(st->rem_ik))
         return DSA_ERR_ARG;
-    if (ratio != kRatio || st->ratio != kRatio) return DSA_ERR_SHAPE;
+    if (!valid_ratio(ratio) || st->ratio != ratio) return DSA_ERR_SHAPE;
     if (st->n_pooled_kv != st->n_pooled_ik) return DSA_ERR_DIVERGED;
-    if (st->n_rem < 0 || st->n_rem >= kRatio || st->n_pooled_kv < 0 ||
-        st->n_pooled_kv * kRatio + st->n_rem != st->n_tokens)
+    if (st->n_rem < 0 || st->n_rem >= ratio || st->n_pooled_kv < 0 ||
+        st->n_pooled_kv * ratio + st->n_rem != st->n_tokens)
         return DSA_ERR_ARG;
     if (offset != st->n_tokens) return DSA_ERR_OFFSET;
     const int64_t end = offset + chunk;
-    const int64_t n_new = end / kRatio;
+    const int64_t n_new = end / ratio;
     if (n_new > st->cap) return DSA_ERR_CAPACITY;
     int rc = launch_pool_append(*st, raw_kv, raw_ik, chunk, offset,
                                 static_cast<cudaStream_t>(stream));
     if (rc != DSA_OK) return rc;
     st->n_pooled_kv = st->n_pooled_ik = n_new;
     st->n_tokens = end;
-    st->n_rem = static_cast<int32_t>(end % kRatio);
+    st->n_rem = static_cast<int32_t>(end % ratio);
     return DSA_OK;
 }
 
@@ -208,7 +214,8 @@ extern "C" const char *dsa_strerror(int code) {
     switch (code) {
         case DSA_OK: return "ok";
         case DSA_ERR_ARG: return "invalid argument (null, non-positive size or misaligned pointer)";
-        case DSA_ERR_SHAPE: return "unsupported shape (ratio, index_topk, window or tile)";
+        case DSA_ERR_SHAPE:
+            return "unsupported shape (ratio not a power of two in [2,128], index_topk, window or tile)";
         case DSA_ERR_OFFSET: return "chunk offset does not match the tokens already in the cache";
         case DSA_ERR_CAPACITY: return "pooled cache capacity exceeded";
         case DSA_ERR_DIVERGED: return "attention and indexer pooled caches hold different row counts";

@@ -13,8 +13,8 @@ int check_score_topk(const void *q_idx, const float *w, const void *pooled_ik, i
                      int64_t chunk, int64_t offset, int32_t ratio, int32_t k, int64_t tile_rows,
                      const void *scratch, size_t scratch_bytes, const int32_t *sel);
 int run_score_topk(const void *q_idx, const float *w, const void *pooled_ik, int64_t n,
-                   int64_t chunk, int64_t offset, int32_t k, int64_t tile_rows, void *scratch,
-                   int32_t *sel, int32_t *status, cudaStream_t s);
+                   int64_t chunk, int64_t offset, int32_t ratio, int32_t k, int64_t tile_rows,
+                   void *scratch, int32_t *sel, int32_t *status, cudaStream_t s);
 int check_attention(const void *q, const void *raw_kv, int64_t raw_start, int64_t raw_rows,
                     const void *pooled_kv, int64_t n, const int32_t *sel, int32_t k,
                     int64_t chunk, int64_t offset, int32_t ratio, int32_t window, float scale,
@@ -33,20 +33,21 @@ extern "C" int dsa_prefill_chunk(dsa_pool_state *st, const void *raw_kv, int64_t
     if (!aligned16(raw_ik) || !aligned16(st->pooled_kv) || !aligned16(st->pooled_ik) ||
         !aligned16(st->rem_kv) || !aligned16(st->rem_ik))
         return DSA_ERR_ARG;
-    if (st->ratio != kRatio) return DSA_ERR_SHAPE;
+    const int32_t ratio = st->ratio;
+    if (!valid_ratio(ratio)) return DSA_ERR_SHAPE;
     if (st->n_pooled_kv != st->n_pooled_ik) return DSA_ERR_DIVERGED;
-    if (st->n_rem < 0 || st->n_rem >= kRatio || st->n_pooled_kv < 0 ||
-        st->n_pooled_kv * kRatio + st->n_rem != st->n_tokens)
+    if (st->n_rem < 0 || st->n_rem >= ratio || st->n_pooled_kv < 0 ||
+        st->n_pooled_kv * ratio + st->n_rem != st->n_tokens)
         return DSA_ERR_ARG;
     if (offset != st->n_tokens) return DSA_ERR_OFFSET;
     const int64_t end = offset + chunk;
-    const int64_t n = end / kRatio;
+    const int64_t n = end / ratio;
     if (n > st->cap) return DSA_ERR_CAPACITY;
-    int rc = check_score_topk(q_idx, w, st->pooled_ik, n, chunk, offset, kRatio, index_topk,
+    int rc = check_score_topk(q_idx, w, st->pooled_ik, n, chunk, offset, ratio, index_topk,
                               tile_rows, scratch, scratch_bytes, sel);
     if (rc != DSA_OK) return rc;
     rc = check_attention(q, raw_kv, raw_start, raw_rows, st->pooled_kv, n, sel, index_topk, chunk,
-                         offset, kRatio, window, scale, out);
+                         offset, ratio, window, scale, out);
     if (rc != DSA_OK) return rc;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
@@ -56,10 +57,10 @@ extern "C" int dsa_prefill_chunk(dsa_pool_state *st, const void *raw_kv, int64_t
     if (rc != DSA_OK) return rc;
     st->n_pooled_kv = st->n_pooled_ik = n;
     st->n_tokens = end;
-    st->n_rem = static_cast<int32_t>(end % kRatio);
-    rc = run_score_topk(q_idx, w, st->pooled_ik, n, chunk, offset, index_topk, tile_rows, scratch,
-                        sel, dev_status, s);
+    st->n_rem = static_cast<int32_t>(end % ratio);
+    rc = run_score_topk(q_idx, w, st->pooled_ik, n, chunk, offset, ratio, index_topk, tile_rows,
+                        scratch, sel, dev_status, s);
     if (rc != DSA_OK) return rc;
     return launch_attention(q, raw_kv, raw_start, raw_rows, st->pooled_kv, n, sel, index_topk,
-                            chunk, offset, window, scale, out, dev_status, s);
+                            chunk, offset, ratio, window, scale, out, dev_status, s);
 }

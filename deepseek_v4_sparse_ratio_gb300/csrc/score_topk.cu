@@ -58,6 +58,7 @@ struct ScoreParams {
     int64_t stride;   // floats per scratch row (multiple of 128)
     int64_t n;        // pooled rows
     int64_t offset;   // absolute position of chunk row 0
+    int32_t ratio;    // raw tokens per pooled row
     int64_t r0;       // first chunk row of the tile
     int R;            // rows in the tile
     int nseg;         // key-range segments per 8-row group
@@ -76,7 +77,7 @@ __device__ __forceinline__ Unit unit_geom(const ScoreParams &p, int u) {
     x.row0 = g * kTok;
     x.nrow = min(kTok, p.R - x.row0);
     const int64_t t_last = p.offset + p.r0 + x.row0 + x.nrow - 1;
-    const int64_t nv = min(p.n, (t_last + 1) / kRatio);
+    const int64_t nv = min(p.n, (t_last + 1) / p.ratio);
     const int kb_vis = static_cast<int>((nv + kScoreBlock - 1) / kScoreBlock);
     x.b0 = static_cast<int>(static_cast<int64_t>(s) * p.NB / p.nseg);
     x.b1 = static_cast<int>(static_cast<int64_t>(s + 1) * p.NB / p.nseg);
@@ -95,7 +96,7 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
 __device__ __forceinline__ void store_score(const ScoreParams &p, int row, int64_t j, float acc) {
     if (row >= p.R) return;
     const int64_t t = p.offset + p.r0 + row;
-    const int64_t nv = min(p.n, (t + 1) / kRatio);
+    const int64_t nv = min(p.n, (t + 1) / p.ratio);
     // sum of (+0) and (-0) terms can be -0; keep one zero so key order is total
     const float s = j < nv ? (acc == 0.0f ? 0.0f : acc) : -INFINITY;
     __stcs(p.scores + static_cast<int64_t>(row) * p.stride + j, s);
@@ -408,7 +409,7 @@ __device__ __forceinline__ void radix_select(KeyAt key_at, int64_t count, uint32
 // segments (coalesced, and the last pass must emit in index order).
 __global__ void __launch_bounds__(kTopkThreads)
     topk_kernel(const float *__restrict__ scores, int64_t stride, int64_t n, int64_t offset,
-                int64_t r0, int32_t k, int32_t *__restrict__ sel) {
+                int32_t ratio, int64_t r0, int32_t k, int32_t *__restrict__ sel) {
     __shared__ uint32_t hist[kBins];
     __shared__ uint32_t cand[kCandCap];
     __shared__ int32_t cand_j[kCandCap];
@@ -420,7 +421,7 @@ __global__ void __launch_bounds__(kTopkThreads)
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int row = blockIdx.x;
     const int64_t t = offset + r0 + row;
-    const int64_t L = min(n, (t + 1) / kRatio);
+    const int64_t L = min(n, (t + 1) / ratio);
     int32_t *out = sel + (r0 + row) * static_cast<int64_t>(k);
     if (L <= k) {
         for (int i = threadIdx.x; i < k; i += kTopkThreads) out[i] = i < L ? i : -1;
@@ -551,12 +552,12 @@ __global__ void __launch_bounds__(kTopkThreads)
 
 // Selection without scoring: sel[i, c] = c if c < n_vis(t) else -1 (n = 0: all -1).
 __global__ void fill_selection_kernel(int32_t *sel, int64_t rows, int32_t k, int64_t offset,
-                                      int64_t n) {
+                                      int64_t n, int32_t ratio) {
     const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (idx >= rows * k) return;
     const int64_t i = idx / k;
     const int32_t c = static_cast<int32_t>(idx % k);
-    const int64_t nv = min(n, (offset + i + 1) / kRatio);
+    const int64_t nv = min(n, (offset + i + 1) / ratio);
     sel[idx] = c < nv ? c : -1;
 }
 
@@ -578,16 +579,16 @@ int choose_segments(int groups, int NB, int sms) {
 }  // namespace
 
 int launch_fill_selection(int32_t *sel, int64_t rows, int32_t k, int64_t offset, int64_t n,
-                          cudaStream_t s) {
+                          int32_t ratio, cudaStream_t s) {
     const int64_t total = rows * k;
-    fill_selection_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, s>>>(sel, rows, k,
-                                                                                   offset, n);
+    fill_selection_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, s>>>(
+        sel, rows, k, offset, n, ratio);
     return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
 int launch_score_tile(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const float *w, int64_t n,
-                      int64_t offset, int64_t r0, int64_t R, float *scores, int64_t stride,
-                      int32_t *status, cudaStream_t s) {
+                      int64_t offset, int32_t ratio, int64_t r0, int64_t R, float *scores,
+                      int64_t stride, int32_t *status, cudaStream_t s) {
     static bool attr_set = false;
     if (!attr_set) {
         if (cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -602,6 +603,7 @@ int launch_score_tile(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const fl
     p.stride = stride;
     p.n = n;
     p.offset = offset;
+    p.ratio = ratio;
     p.r0 = r0;
     p.R = static_cast<int>(R);
     p.NB = static_cast<int>(stride / kScoreBlock);
@@ -614,11 +616,12 @@ int launch_score_tile(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const fl
     return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
-int launch_topk_tile(const float *scores, int64_t stride, int64_t n, int64_t offset, int64_t r0,
-                     int64_t R, int32_t k, int32_t *sel, int32_t *status, cudaStream_t s) {
+int launch_topk_tile(const float *scores, int64_t stride, int64_t n, int64_t offset,
+                     int32_t ratio, int64_t r0, int64_t R, int32_t k, int32_t *sel,
+                     int32_t *status, cudaStream_t s) {
     (void)status;
-    topk_kernel<<<static_cast<unsigned>(R), kTopkThreads, 0, s>>>(scores, stride, n, offset, r0, k,
-                                                                 sel);
+    topk_kernel<<<static_cast<unsigned>(R), kTopkThreads, 0, s>>>(scores, stride, n, offset, ratio,
+                                                                 r0, k, sel);
     return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
@@ -627,8 +630,8 @@ int check_score_topk(const void *q_idx, const float *w, const void *pooled_ik, i
                      int64_t chunk, int64_t offset, int32_t ratio, int32_t k, int64_t tile_rows,
                      const void *scratch, size_t scratch_bytes, const int32_t *sel) {
     if (!sel || chunk <= 0 || offset < 0 || n < 0) return DSA_ERR_ARG;
-    if (ratio != kRatio || k <= 0 || tile_rows <= 0) return DSA_ERR_SHAPE;
-    if (n != (offset + chunk) / kRatio) return DSA_ERR_ARG;
+    if (!valid_ratio(ratio) || k <= 0 || tile_rows <= 0) return DSA_ERR_SHAPE;
+    if (n != (offset + chunk) / ratio) return DSA_ERR_ARG;
     if (!aligned16(sel)) return DSA_ERR_ARG;
     if (n > k) {
         if (!q_idx || !w || !pooled_ik || !aligned16(q_idx) || !aligned16(w) ||
@@ -643,9 +646,9 @@ int check_score_topk(const void *q_idx, const float *w, const void *pooled_ik, i
 }
 
 int run_score_topk(const void *q_idx, const float *w, const void *pooled_ik, int64_t n,
-                   int64_t chunk, int64_t offset, int32_t k, int64_t tile_rows, void *scratch,
-                   int32_t *sel, int32_t *status, cudaStream_t s) {
-    if (n == 0 || n <= k) return launch_fill_selection(sel, chunk, k, offset, n, s);
+                   int64_t chunk, int64_t offset, int32_t ratio, int32_t k, int64_t tile_rows,
+                   void *scratch, int32_t *sel, int32_t *status, cudaStream_t s) {
+    if (n == 0 || n <= k) return launch_fill_selection(sel, chunk, k, offset, n, ratio, s);
     CUtensorMap tm_q, tm_k;
     if (!make_tmap_bf16(&tm_q, q_idx, kDI, static_cast<uint64_t>(chunk) * kHI, kDI * 2, 64, 256))
         return DSA_ERR_CUDA;
@@ -655,9 +658,10 @@ int run_score_topk(const void *q_idx, const float *w, const void *pooled_ik, int
     float *scores = static_cast<float *>(scratch);
     for (int64_t r0 = 0; r0 < chunk; r0 += tile_rows) {
         const int64_t R = std::min(tile_rows, chunk - r0);
-        int rc = launch_score_tile(tm_q, tm_k, w, n, offset, r0, R, scores, stride, status, s);
+        int rc =
+            launch_score_tile(tm_q, tm_k, w, n, offset, ratio, r0, R, scores, stride, status, s);
         if (rc != DSA_OK) return rc;
-        rc = launch_topk_tile(scores, stride, n, offset, r0, R, k, sel, status, s);
+        rc = launch_topk_tile(scores, stride, n, offset, ratio, r0, R, k, sel, status, s);
         if (rc != DSA_OK) return rc;
     }
     return DSA_OK;
@@ -680,8 +684,8 @@ extern "C" int dsa_index_score_topk(const void *q_idx, const float *w, const voi
     int rc = check_score_topk(q_idx, w, pooled_ik, n_pooled, chunk, offset, ratio, index_topk,
                               tile_rows, scratch, scratch_bytes, sel);
     if (rc != DSA_OK) return rc;
-    return run_score_topk(q_idx, w, pooled_ik, n_pooled, chunk, offset, index_topk, tile_rows,
-                          scratch, sel, dev_status, static_cast<cudaStream_t>(stream));
+    return run_score_topk(q_idx, w, pooled_ik, n_pooled, chunk, offset, ratio, index_topk,
+                          tile_rows, scratch, sel, dev_status, static_cast<cudaStream_t>(stream));
 }
 
 // ------------------------------------------------------------------ no-allocation variant
@@ -733,6 +737,6 @@ extern "C" int dsa_index_score_topk_noalloc(const void *q_idx, const float *w,
         rc = static_scratch(&scratch);
         if (rc != DSA_OK) return rc;
     }
-    return run_score_topk(q_idx, w, pooled_ik, n_pooled, chunk, offset, index_topk, tile_rows,
-                          scratch, sel, dev_status, static_cast<cudaStream_t>(stream));
+    return run_score_topk(q_idx, w, pooled_ik, n_pooled, chunk, offset, ratio, index_topk,
+                          tile_rows, scratch, sel, dev_status, static_cast<cudaStream_t>(stream));
 }

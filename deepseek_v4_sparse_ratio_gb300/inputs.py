@@ -109,17 +109,26 @@ def workload(name: str) -> Workload:
         off = 1048576 - 4096
         return Workload(name, 4, [4096], off, off // RATIO, index_topk=2048,
                         window=128, sample_rows=128, tile_rows=(1024, 4096))
+    # compressed attention (ratio 128): every visible pooled row plus the window
+    if name == "compressed_16k":
+        return Workload(name, 5, [2048] * 8, 0, 0, index_topk=128, window=128, ratio=128,
+                        sample_rows=64, tile_rows=(2048,))
+    if name == "compressed_128k":
+        off = 131072 - 4096
+        return Workload(name, 6, [4096], off, off // 128, index_topk=1024, window=128,
+                        ratio=128, sample_rows=128, tile_rows=(4096,))
     raise KeyError(name)
 
 
 WORKLOADS = ("zero_prefix_512", "two_chunks_4098", "prompt_16k", "ctx_128k", "ctx_1m")
+COMPRESSED_WORKLOADS = ("compressed_16k", "compressed_128k")
 
 
 def small(seed: int, chunks, index_topk: int, window: int = 128, off0: int = 0,
-          prefix_pooled: int = 0, name: str = "small") -> Workload:
+          prefix_pooled: int = 0, name: str = "small", ratio: int = RATIO) -> Workload:
     """A custom small workload with the same distributions."""
     return Workload(name, seed, list(chunks), off0, prefix_pooled,
-                    index_topk=index_topk, window=window)
+                    index_topk=index_topk, window=window, ratio=ratio)
 
 
 def sample_rows(T: int, S: int):

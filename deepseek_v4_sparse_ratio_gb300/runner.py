@@ -29,13 +29,13 @@ class DeviceWorkload:
         self.q_idx = t["q_idx"].to(dev).contiguous()
         self.w = t["w"].to(dev).contiguous()
         self.q = t["q"].to(dev).contiguous()
-        self.cap = wl.end // B.RATIO
+        self.cap = wl.end // wl.ratio
         self.prefix_ik = t["prefix_ik"].to(dev) if wl.off0 else None
         self.prefix_kv = t["prefix_kv"].to(dev) if wl.off0 else None
         self.tmax = max(wl.chunks)
         self.k = wl.index_topk
         self.tile_rows = tile_rows or (wl.tile_rows[0] if wl.tile_rows else self.tmax)
-        n_final = wl.end // B.RATIO
+        n_final = wl.end // wl.ratio
         nbytes = B.dsa_score_scratch_bytes(min(self.tile_rows, self.tmax), n_final)
         self.scratch = torch.empty(max(nbytes // 4, 1), dtype=torch.float32, device=dev)
         self.sel = torch.empty(self.tmax, self.k, dtype=torch.int32, device=dev)
@@ -48,9 +48,9 @@ class DeviceWorkload:
         """Fresh PoolingCache at the workload's starting offset."""
         if self.wl.off0:
             self.state = B.PoolState.from_prefix(self.prefix_ik, self.prefix_kv, self.wl.off0,
-                                                 self.cap, self.device)
+                                                 self.cap, self.device, self.wl.ratio)
         else:
-            self.state = B.PoolState(self.cap, self.device)
+            self.state = B.PoolState(self.cap, self.device, self.wl.ratio)
 
     def run_chunk(self, c: int, stream=None) -> None:
         _, s, T, off = list(self.wl.chunk_bounds())[c]

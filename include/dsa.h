@@ -14,7 +14,9 @@
  *
  * Shapes are fixed by the model: indexer heads H_I=64 of dim d_I=128, query
  * heads H=64, one shared KV row of dim D=512 (key and value for every head),
- * B=1, bf16 storage, fp32 accumulation. Only ratio 4 is accepted.
+ * B=1, bf16 storage, fp32 accumulation. The pooling ratio is a power of two
+ * in [2, 128]: 4 for the indexed (sparse) attention, 128 for the compressed
+ * attention whose selection is every visible pooled row (index_topk >= n).
  *
  * Conventions for every call:
  *   - All tensor pointers are DEVICE pointers to row-major, densely packed
@@ -55,7 +57,7 @@ extern "C" {
 enum dsa_status {
     DSA_OK = 0,
     DSA_ERR_ARG = -1,       /* null pointer, non-positive size, misaligned pointer */
-    DSA_ERR_SHAPE = -2,     /* ratio != 4, index_topk <= 0, window <= 0, bad tile */
+    DSA_ERR_SHAPE = -2,     /* bad ratio, index_topk <= 0, window <= 0, bad tile */
     DSA_ERR_OFFSET = -3,    /* offset != tokens already in the cache */
     DSA_ERR_CAPACITY = -4,  /* the append would exceed the preallocated cache */
     DSA_ERR_DIVERGED = -5,  /* KV and indexer caches hold different row counts */
@@ -79,7 +81,7 @@ enum dsa_status {
  *   pooled_kv [cap, 512] bf16, pooled_ik [cap, 128] bf16,
  *   rem_kv    [ratio-1, 512] bf16, rem_ik [ratio-1, 128] bf16 (raw remainder rows,
  *             slot s = token n_pooled*ratio + s).
- * A fresh cache has all counters 0 and ratio = 4. To resume from a prefix,
+ * A fresh cache has all counters 0 and its ratio set. To resume from a prefix,
  * fill the first n_pooled rows and set n_tokens = n_pooled*ratio + n_rem.
  * Snapshot/rollback = copy this struct (and the n_rem remainder rows).
  */
@@ -93,19 +95,20 @@ typedef struct dsa_pool_state {
     int64_t n_pooled_ik;  /* pooled rows held in pooled_ik */
     int64_t n_tokens;     /* raw tokens consumed so far = absolute offset of the next chunk */
     int32_t n_rem;        /* raw remainder rows held (n_tokens mod ratio) */
-    int32_t ratio;        /* 4 */
+    int32_t ratio;        /* raw tokens per pooled row: 4 (indexed) or 128 (compressed) */
 } dsa_pool_state;
 
 /*
  * (a) Pool and append one chunk.
  * Cites: the first page's Summary/Correctness (compressor runs once per chunk
  * in both paths; remainder); the second page's Summary item 4 (in-place append).
- * Reading taken: pooled row = mean of its `ratio` raw rows, computed exactly
- * and rounded once to bf16 (round to nearest, ties to even).
+ * Reading taken: pooled row = mean of its `ratio` raw rows, summed in row
+ * order in fp64 (exact for bf16 inputs of ordinary range), divided by the
+ * ratio and rounded once to bf16 (round to nearest, ties to even).
  *
  *   raw_kv [chunk, 512] bf16, raw_ik [chunk, 128] bf16: the chunk's raw rows.
  *   chunk > 0; offset must equal st->n_tokens (else DSA_ERR_OFFSET);
- *   ratio must equal st->ratio == 4.
+ *   ratio must equal st->ratio, a power of two in [2, 128].
  * Writes pooled rows [n_old, n_new) of both caches and the new remainder, then
  * sets n_pooled_kv = n_pooled_ik = n_new = floor((offset+chunk)/ratio),
  * n_tokens = offset+chunk, n_rem = (offset+chunk) mod ratio.
@@ -140,7 +143,8 @@ size_t dsa_score_scratch_bytes(int64_t tile_rows, int64_t n_pooled);
  *
  *   q_idx [chunk, 64, 128] bf16; w [chunk, 64] fp32; pooled_ik [>= n_pooled, 128] bf16;
  *   n_pooled = n after this chunk's append; chunk > 0; offset >= 0 with
- *   n_pooled == floor((offset+chunk)/ratio); index_topk > 0;
+ *   n_pooled == floor((offset+chunk)/ratio); ratio a power of two in [2, 128];
+ *   index_topk > 0;
  *   tile_rows > 0 (query rows per score/top-k tile; any value gives the same result);
  *   scratch: device buffer of scratch_bytes >= dsa_score_scratch_bytes(min(tile_rows,
  *   chunk), n_pooled) -- only touched on the full path (may be NULL otherwise);

@@ -208,8 +208,9 @@ def test_attention_reports_bad_index_and_skips_it(dsa):
 
 def _oracle_prefix_state(wl):
     if wl.off0:
-        return oracle.PoolState.from_prefix(wl.t["prefix_ik"], wl.t["prefix_kv"], wl.off0)
-    return oracle.PoolState(4)
+        return oracle.PoolState.from_prefix(wl.t["prefix_ik"], wl.t["prefix_kv"], wl.off0,
+                                            wl.ratio)
+    return oracle.PoolState(wl.ratio)
 
 
 def run_workload_parity(wl, tile_rows, sample):
@@ -226,11 +227,11 @@ def run_workload_parity(wl, tile_rows, sample):
                                    off, wl.t["q_idx"][s:s + T], wl.t["w"][s:s + T].numpy(),
                                    wl.t["q"][s:s + T], raw_all, dw.raw_start, rows,
                                    wl.index_topk, wl.window, SCALE)
-        assert dw.state.n_pooled == res["n"] == (off + T) // 4
+        assert dw.state.n_pooled == res["n"] == (off + T) // wl.ratio
         gsel = dw.sel[:T].cpu().numpy()
         sels.append(gsel)
         check_selection(gsel[rows], res["sel"], res["pos"], res["n"], wl.index_topk,
-                        res["scores"], res["mag"])
+                        res["scores"], res["mag"], ratio=wl.ratio)
         same = np.all(gsel[rows] == res["sel"], axis=1)
         check_attention(bf16_to_f64(dw.out[rows]), res["out"], same)
     n = ref_state.n_pooled
