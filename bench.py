@@ -54,13 +54,13 @@ def load_peaks():
 
 def work_counts(wl):
     """Algorithmic work of one step: score flops, attention flops, bytes."""
-    T, off, k, W = wl.chunks[0], wl.off0, wl.index_topk, wl.window
-    n = (off + T) // 4
+    T, off, k, W, r = wl.chunks[0], wl.off0, wl.index_topk, wl.window, wl.ratio
+    n = (off + T) // r
     score_flops = attn_flops = 0
     topk_bytes = 0
     for i in range(T):
         t = off + i
-        nv = min((t + 1) // 4, n)
+        nv = min((t + 1) // r, n)
         score_flops += 2 * 64 * 128 * nv
         topk_bytes += 4 * nv
         attn_flops += 4 * 64 * 512 * (min(W, t + 1) + min(k, nv))
@@ -68,11 +68,39 @@ def work_counts(wl):
             "score_read_bytes": T * 64 * 128 * 2 + T * 64 * 4 + n * 128 * 2,
             "score_write_bytes": 4 * T * ((n + 127) // 128 * 128),
             "topk_bytes": topk_bytes + T * k * 4,
-            "pool_bytes": T * 640 * 2 + (T // 4) * 640 * 2}
+            "pool_bytes": T * 640 * 2 + (T // r) * 640 * 2}
+
+
+# DRAM bytes (read + write) per launch from one ncu capture of each kernel on the
+# ctx_128k workload (dram__bytes_read.sum + dram__bytes_write.sum), with a hash of
+# the sources the captured build came from; a changed source reports null.
+NCU_TRAFFIC = {
+    "attn_kernel": {"bytes": 344.4e6 + 231.8e6, "files": ("attn.cu", "common.cuh", "internal.h"),
+                    "sha256_16": "4b3e408c3581dcdf"},
+    "score_kernel": {"bytes": 76.9e6 + 477.5e6,
+                     "files": ("score_topk.cu", "common.cuh", "internal.h"),
+                     "sha256_16": "53953df26a848e33"},
+    "topk_kernel": {"bytes": 589.1e6 + 31.6e6,
+                    "files": ("score_topk.cu", "common.cuh", "internal.h"),
+                    "sha256_16": "53953df26a848e33"},
+}
+
+
+def ncu_traffic(kernel, workload):
+    """The captured traffic if the kernel's sources are the captured ones, else None."""
+    import hashlib
+    rec = NCU_TRAFFIC.get(kernel)
+    if rec is None or workload != WORKLOAD:
+        return None
+    h = hashlib.sha256()
+    for f in rec["files"]:
+        with open(os.path.join(ROOT, "deepseek_v4_sparse_ratio_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return rec["bytes"] if h.hexdigest()[:16] == rec["sha256_16"] else None
 
 
 class ClockSampler:
-    """nvidia-smi clocks/throttle reasons sampled every 200 ms while running."""
+    """nvidia-smi clocks/throttle reasons sampled every 100 ms while running."""
 
     def __init__(self, index: int):
         self.index = index
@@ -87,7 +115,7 @@ class ClockSampler:
         try:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.index), f"--query-gpu={q}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
                                          stdout=self.fh, stderr=subprocess.DEVNULL)
         except Exception:
             self.proc = None
@@ -151,13 +179,18 @@ def max_over_ranks(x, world, device):
     return float(t.item())
 
 
-def cpu_baseline(wl, seconds_budget: float = 20.0, max_rows: int = 256):
+def job_throughput(units_per_rank, world, ms):
+    """Whole-job rate: the units all ranks processed / the slowest rank's step time."""
+    return world * units_per_rank / (ms * 1e-3)
+
+
+def cpu_baseline(wl, seconds_budget: float = 20.0, max_rows: int = 4096):
     """The oracle, as it stands, on sampled query rows of the workload."""
     import numpy as np
     import oracle
     from deepseek_v4_sparse_ratio_gb300 import inputs
     T, off = wl.chunks[0], wl.off0
-    st = oracle.PoolState.from_prefix(wl.t["prefix_ik"], wl.t["prefix_kv"], off)
+    st = oracle.PoolState.from_prefix(wl.t["prefix_ik"], wl.t["prefix_kv"], off, wl.ratio)
     t0 = time.perf_counter()
     st.append(wl.t["raw_ik"], wl.t["raw_kv"], off)
     t_pool = time.perf_counter() - t0
@@ -171,7 +204,7 @@ def cpu_baseline(wl, seconds_budget: float = 20.0, max_rows: int = 256):
         pos = off + np.asarray(rows)
         t0 = time.perf_counter()
         sel, _, _ = oracle.select(oracle.as_bf16_bits(wl.t["q_idx"])[rows],
-                                  wl.t["w"].numpy()[rows], pos, st.pooled_ik, st.n_pooled, 4,
+                                  wl.t["w"].numpy()[rows], pos, st.pooled_ik, st.n_pooled, wl.ratio,
                                   wl.index_topk)
         oracle.attention(oracle.as_bf16_bits(wl.t["q"])[rows], pos, raw_all, raw_start,
                          st.pooled_kv, st.n_pooled, sel, wl.window, 1 / math.sqrt(512))
@@ -199,7 +232,7 @@ def run_reference(args):
     wl = inputs.draw(inputs.workload(WORKLOAD))
     T, off = wl.chunks[0], wl.off0
     oracle.build()
-    base = oracle.PoolState.from_prefix(wl.t["prefix_ik"], wl.t["prefix_kv"], off)
+    base = oracle.PoolState.from_prefix(wl.t["prefix_ik"], wl.t["prefix_kv"], off, wl.ratio)
     raw_all = __import__("torch").cat([wl.t["prefix_win"], wl.t["raw_kv"]], 0)
     raw_start = off - wl.t["prefix_win"].shape[0]
     rows_per_step = args.ref_rows
@@ -210,7 +243,7 @@ def run_reference(args):
         rows = [(i * 997 + r * (T // rows_per_step)) % T for r in range(rows_per_step)]
         pos = off + np.asarray(rows)
         sel, _, _ = oracle.select(oracle.as_bf16_bits(wl.t["q_idx"])[rows],
-                                  wl.t["w"].numpy()[rows], pos, st.pooled_ik, st.n_pooled, 4,
+                                  wl.t["w"].numpy()[rows], pos, st.pooled_ik, st.n_pooled, wl.ratio,
                                   wl.index_topk)
         oracle.attention(oracle.as_bf16_bits(wl.t["q"])[rows], pos, raw_all, raw_start,
                          st.pooled_kv, st.n_pooled, sel, wl.window, 1 / math.sqrt(512))
@@ -239,8 +272,8 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--tile-rows", type=int, default=0)
@@ -274,7 +307,8 @@ def main():
     flush = torch.empty(512 * 2 ** 20 // 4, dtype=torch.float32, device=dev)
     snap = dw.state.snapshot()
     counts = work_counts(wl)
-    n = (wl.off0 + T) // 4
+    r = wl.ratio
+    n = (wl.off0 + T) // r
 
     def step():
         dw.state.restore(snap)
@@ -305,7 +339,7 @@ def main():
     dw.check_status()
     step_ms = [a.elapsed_time(b) for a, b in ev]
     ms = max_over_ranks(sum(step_ms) / len(step_ms), world, dev)
-    value = world * T / (ms * 1e-3)
+    value = job_throughput(T, world, ms)
 
     # ---- per-component times: the same calls one ABI entry point at a time
     comp = {"pool": [], "score_topk": [], "attention": []}
@@ -315,13 +349,13 @@ def main():
         dw.state.restore(snap)
         e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
         e[0].record(stream)
-        B.dsa_pool_append(dw.state, dw.raw_kv[off - dw.raw_start:], dw.raw_ik, T, off, 4, stream)
+        B.dsa_pool_append(dw.state, dw.raw_kv[off - dw.raw_start:], dw.raw_ik, T, off, r, stream)
         e[1].record(stream)
-        B.dsa_index_score_topk(dw.q_idx, dw.w, dw.state.pooled_ik, n, T, off, 4, k, tile,
+        B.dsa_index_score_topk(dw.q_idx, dw.w, dw.state.pooled_ik, n, T, off, r, k, tile,
                                dw.scratch, dw.sel, dw.status, stream)
         e[2].record(stream)
         B.dsa_window_sparse_attn(dw.q, dw.raw_kv, dw.raw_start, dw.state.pooled_kv, n, dw.sel, k,
-                                 T, off, 4, wl.window, dw.scale, dw.out, dw.status, stream)
+                                 T, off, r, wl.window, dw.scale, dw.out, dw.status, stream)
         e[3].record(stream)
         torch.cuda.synchronize()
         if i >= 1:
@@ -361,30 +395,52 @@ def main():
             torch.cuda.synchronize()
             ee.append(a.elapsed_time(b))
         ems = max_over_ranks(statistics.mean(ee), world, dev)
-        e2e = {"value": world * T / (ems * 1e-3), "unit": UNIT, "h2d_bytes_per_step": h2d,
+        e2e = {"value": job_throughput(T, world, ems), "unit": UNIT, "h2d_bytes_per_step": h2d,
                "d2h_bytes_per_step": d2h, "ms_per_step": ems}
 
     peaks, src = load_peaks()
-    t_st = comp_ms["score_topk"] * 1e-3
-    achieved = counts["score_flops"] / t_st / 1e12
+    # every kernel here is timed alone (one ABI call between events): burst peaks
+    peak_tf, peak_bw = peaks["bf16_tflops"], peaks["hbm_gbs"]
     attn_tf = counts["attn_flops"] / (comp_ms["attention"] * 1e-3) / 1e12
+    st_tf = counts["score_flops"] / (comp_ms["score_topk"] * 1e-3) / 1e12
+    attn_traffic = ncu_traffic("attn_kernel", args.workload)
+    skip = n <= wl.index_topk
+    n_tiles = 0 if skip else math.ceil(T / tile)
+    launches_per_step = (1 + (1 if (wl.off0 + T) % r else 0)   # pool (+ remainder)
+                         + (1 if skip else 2 * n_tiles)          # fill, or score+top-k per tile
+                         + 1)                                    # attention
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD_DESC, "name": wl.name, "chunk": T, "context": wl.end,
+        "config": {"workload": WORKLOAD_DESC if args.workload == WORKLOAD else args.workload,
+                   "name": wl.name, "chunk": T, "context": wl.end, "ratio": r,
                    "index_topk": wl.index_topk, "tile_rows": tile, "pooled_rows": n,
                    "l2": "flushed between steps (512 MiB write, outside the step events)",
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
-        "roofline": {"kernel": "indexer score + top-k (dsa_index_score_topk)", "bound": "tensor",
-                     "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
-                     "frac": achieved / peaks["bf16_tflops"], "traffic": None,
+        # the dominant kernel of the step (about half of its time): window + selected
+        # attention, one attn_kernel launch per dsa_window_sparse_attn call
+        "roofline": {"kernel": "attn_kernel (dsa_window_sparse_attn)", "bound": "tensor",
+                     "achieved": attn_tf, "peak": peak_tf, "unit": "TFLOP/s",
+                     "frac": attn_tf / peak_tf,
+                     "traffic": attn_traffic,
                      "peak_source": f"{src} bf16 dense (burst)",
-                     "algorithmic_flops_per_launch": counts["score_flops"]},
+                     "algorithmic_flops_per_launch": counts["attn_flops"],
+                     "ms_per_launch": comp_ms["attention"]},
+        # the fused indexer step: score kernel + top-k kernel of each tile
+        "score_topk_roofline": {"kernel": "score_kernel + topk_kernel (dsa_index_score_topk)",
+                                "bound": "tensor", "achieved": st_tf, "peak": peak_tf,
+                                "unit": "TFLOP/s", "frac": st_tf / peak_tf,
+                                "traffic": (None if ncu_traffic("score_kernel", args.workload) is None
+                                            else ncu_traffic("score_kernel", args.workload)
+                                            + ncu_traffic("topk_kernel", args.workload)),
+                                "peak_source": f"{src} bf16 dense (burst)",
+                                "algorithmic_flops_per_launch": counts["score_flops"],
+                                "ms_per_call": comp_ms["score_topk"],
+                                "topk_algorithmic_bytes": counts["topk_bytes"],
+                                "hbm_peak_gbs": peak_bw},
         "components_ms": comp_ms,
-        "attention_roofline": {"achieved": attn_tf, "unit": "TFLOP/s",
-                               "frac": attn_tf / peaks["bf16_tflops"], "bound": "tensor"},
-        "gpu_launches": args.steps * (2 + 2 * math.ceil(T / tile)),
+        "gpu_launches": args.steps * launches_per_step,
         "clocks": clk.summary(),
         "wall_s_timed_region": wall,
     }

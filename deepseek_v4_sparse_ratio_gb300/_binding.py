@@ -23,7 +23,7 @@ DSA_ERR_BOUNDS, DSA_ERR_RAW_RANGE = -9, -10
 
 EXPORTS = ("dsa_pool_append", "dsa_score_scratch_bytes", "dsa_index_score_topk",
            "dsa_window_sparse_attn", "dsa_prefill_chunk", "dsa_strerror",
-           "dsa_index_score_topk_noalloc")
+           "dsa_index_score_topk_noalloc", "dsa_bounded_wait_selftest")
 DSA_STATIC_SCRATCH_BYTES = 16 << 20
 
 
@@ -62,10 +62,11 @@ def load(path: str | None = None):
     lib.dsa_prefill_chunk.argtypes = [S, P, i64, i64, P, P, P, P, i64, i64, i32, i32,
                                       ctypes.c_float, i64, P, sz, P, P, P, P]
     lib.dsa_index_score_topk_noalloc.argtypes = [P, P, P, i64, i64, i64, i32, i32, i64, P, P, P]
+    lib.dsa_bounded_wait_selftest.argtypes = [i32, P, P]
     lib.dsa_strerror.argtypes = [ctypes.c_int]
     lib.dsa_strerror.restype = ctypes.c_char_p
     for f in ("dsa_pool_append", "dsa_index_score_topk", "dsa_window_sparse_attn",
-              "dsa_prefill_chunk", "dsa_index_score_topk_noalloc"):
+              "dsa_prefill_chunk", "dsa_index_score_topk_noalloc", "dsa_bounded_wait_selftest"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -180,6 +181,12 @@ def dsa_index_score_topk_noalloc(q_idx, w, pooled_ik, n_pooled: int, chunk: int,
                                              offset, ratio, index_topk, tile_rows, _p(sel),
                                              _p(dev_status), _s(stream))
     _check(rc, "dsa_index_score_topk_noalloc")
+
+
+def dsa_bounded_wait_selftest(arrive: bool, dev_status, stream=None) -> None:
+    """Run the library's bounded mbarrier wait on a barrier that gets its arrival or none."""
+    rc = load().dsa_bounded_wait_selftest(1 if arrive else 0, _p(dev_status), _s(stream))
+    _check(rc, "dsa_bounded_wait_selftest")
 
 
 def dsa_window_sparse_attn(q, raw_kv, raw_start: int, pooled_kv, n_pooled: int, sel,

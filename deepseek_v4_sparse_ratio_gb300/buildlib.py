@@ -17,7 +17,7 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libdsa.so")
-SOURCES = ["pool.cu", "score_topk.cu", "attn.cu", "prefill.cu"]
+SOURCES = ["pool.cu", "score_topk.cu", "attn.cu", "prefill.cu", "diag.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 
 

@@ -250,6 +250,25 @@ int dsa_index_score_topk_noalloc(const void *q_idx, const float *w, const void *
                                  int32_t index_topk, int64_t tile_rows, int32_t *sel,
                                  int32_t *dev_status, void *stream);
 
+/*
+ * Self-check of the error path behind DSA_ERR_TIMEOUT, for failure detection.
+ * Every kernel of this library waits on shared-memory mbarriers with a bounded
+ * wait: after about 2^31 SM cycles (about a second) it gives up, records
+ * DSA_ERR_TIMEOUT in dev_status, lets the other warps of its CTA leave, and
+ * the kernel returns, so the CUDA context stays usable. This call launches one
+ * 32-thread CTA that initialises an mbarrier expecting one arrival and waits on
+ * it with that same bounded wait:
+ *   arrive != 0: a thread arrives first; the wait completes at once and
+ *                dev_status is left as it is;
+ *   arrive == 0: nothing arrives; about a second later DSA_ERR_TIMEOUT is
+ *                written to dev_status (if it held DSA_OK) and the kernel ends.
+ * dev_status: device int32, caller-owned. Enqueued on `stream`; returns
+ * DSA_ERR_ARG for a null dev_status, DSA_ERR_CUDA if the launch fails.
+ * The pages have no counterpart to this entry point: it is an addition of this
+ * library.
+ */
+int dsa_bounded_wait_selftest(int32_t arrive, int32_t *dev_status, void *stream);
+
 /* Static description of a DSA_* status code. */
 const char *dsa_strerror(int code);
 

@@ -117,3 +117,7 @@ def test_prefill_chunk_validates_everything_first(lib):
     assert f(*args(raw_start=74)) == B.DSA_ERR_RAW_RANGE
     assert f(*args(window=0)) == B.DSA_ERR_SHAPE
     assert (st.n_pooled_kv, st.n_tokens, st.n_rem) == (50, 200, 0)
+
+
+def test_wait_selftest_rejects_null_status(lib):
+    assert lib.dsa_bounded_wait_selftest(0, None, None) == B.DSA_ERR_ARG
