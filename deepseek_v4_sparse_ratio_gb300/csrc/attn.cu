@@ -15,19 +15,22 @@
 // key and value for all 64 heads.
 //
 // tcgen05 design, one token at a time per CTA (persistent over tokens), keys
-// in blocks of 128 rows (window rows by a TMA tile load, selected rows by TMA
-// gather4), everything transposed so the 128 keys sit on the MMA's M:
+// in blocks of 128 rows gathered with cp.async, everything transposed so the
+// 128 keys sit on the MMA's M:
 //   S^T[key, head]  = K_blk[128 x 512] . Q_t^T      (M=128, N=64, K=512)
 //   O^T[d, head]   += V_blk^T[512 x 128] . P^T       (4 x (M=128, N=64, K=128))
 // K_blk and V_blk are the same shared-memory tile (K = V): 8 chunks of
 // [128 rows x 64 dims] with 128-byte swizzle, read K-major by the first MMA and
-// MN-major by the second. S^T (64 columns) and O^T (4 x 64 columns) live in
-// TMEM. Four softmax warps own TMEM lanes = keys: they mask, run the online
-// softmax in the log2 domain (exp2 of scale*log2e*logit - running max) and
-// write P^T as bf16. The running max is only raised when some logit exceeds it
-// by more than 8 (log2 units): P then stays <= 256, and the rescale of O^T
-// and of the partial sums is skipped on most blocks without changing the
-// result (the same max divides out at the end). Output = O^T / sum, bf16.
+// MN-major by the second, filled and released in chunk pairs (one d-tile of
+// the second MMA each) so the next block's rows stream in while PV drains.
+// S^T (64 columns) and O^T (4 x 64 columns) live in TMEM. Roles: six loader
+// warps, one warp issuing QK, one issuing PV, eight softmax warps that own
+// TMEM lanes = keys: they mask, run the online softmax in the log2 domain
+// (exp2 of scale*log2e*logit - running max) and write P^T as bf16. The running
+// max is only raised when some logit exceeds it by more than 8 (log2 units): P
+// then stays <= 256, and the rescale of O^T and of the partial sums is skipped
+// on most blocks without changing the result (the same max divides out at the
+// end). Output = O^T / sum, bf16.
 #include <math.h>
 
 #include <algorithm>
@@ -38,12 +41,19 @@ namespace dsa {
 
 namespace {
 
-// Warpgroups 0-1: loader warps 0-6 and the MMA warp 7; warpgroups 2-3: softmax
-// warps 8-15. setmaxnreg moves registers from the first two warpgroups to the
-// softmax ones: 256*80 + 256*176 = 512*128, the launch allocation (checked on
-// the host before the first launch).
-constexpr int kLoadWarps = 7;
-constexpr int kMmaWarp = 7;
+// Warpgroups 0-1: loader warps 0-5, the QK-issuing warp 6 and the PV-issuing
+// warp 7; warpgroups 2-3: softmax warps 8-15. setmaxnreg moves registers from
+// the first two warpgroups to the softmax ones: 256*80 + 256*176 = 512*128, the
+// launch allocation (checked on the host before the first launch).
+//
+// QK and PV are issued by two different warps: a thread that waits on an
+// mbarrier between MMAs stalls its own issue until the MMAs it queued have been
+// dispatched, so with one issuing thread every wait leaves the tensor pipe
+// empty for a moment. With two, one warp's waits are covered by the other's
+// queued MMAs.
+constexpr int kLoadWarps = 6;
+constexpr int kQkWarp = 6;
+constexpr int kPvWarp = 7;
 constexpr int kSoftWarp0 = 8;
 constexpr int kAttnThreads = 512;
 constexpr int kRegsLaunch = 128;
@@ -164,31 +174,34 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
     uint64_t *q_full = bars + 0;
     uint64_t *q_free = bars + 1;
-    uint64_t *kv_full = bars + 2;   // [8] chunk landed
+    uint64_t *kv_full = bars + 2;   // [4] chunk pair landed
     uint64_t *kv_free = bars + 10;  // [4] chunk pair (d-tile) consumed by PV
     uint64_t *s_full = bars + 14;
     uint64_t *p_full = bars + 15;
     uint64_t *o_full = bars + 16;
     uint64_t *o_free = bars + 17;
-    uint64_t *drain = bars + 18;
-    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 19);
+    uint64_t *drain = bars + 18;    // [2] one per issuing warp
+    uint64_t *pv_done = bars + 20;  // PV of a block complete (P and O^T free again)
+    uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 21);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
         mbar_init(q_free, 1);
-        for (int c = 0; c < 8; ++c) mbar_init(&kv_full[c], 32 * kLoadWarps);  // noinc arrivals
+        for (int m = 0; m < 4; ++m) mbar_init(&kv_full[m], 32 * kLoadWarps);  // noinc arrivals
         for (int m = 0; m < 4; ++m) mbar_init(&kv_free[m], 1);
         mbar_init(s_full, 1);
         mbar_init(p_full, kSoftThreads);
         mbar_init(o_full, 1);
         mbar_init(o_free, 8);
-        mbar_init(drain, 1);
+        mbar_init(&drain[0], 1);
+        mbar_init(&drain[1], 1);
+        mbar_init(pv_done, 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
-    if (warp == kMmaWarp) tmem_alloc(tmem_holder, 512);
+    if (warp == kPvWarp) tmem_alloc(tmem_holder, 512);
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -261,8 +274,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         cp_async16(dst + (2 * m) * 16384, src + (2 * m) * 128);
                         cp_async16(dst + (2 * m + 1) * 16384, src + (2 * m + 1) * 128);
                     }
-                    cp_async_arrive(&kv_full[2 * m]);
-                    cp_async_arrive(&kv_full[2 * m + 1]);
+                    cp_async_arrive(&kv_full[m]);
                     if (m == 0)
                         jn = (b + 1 < x.nb) ? fetch(x, i, b + 1)
                                             : (inext < p.T ? fetch(xnext, inext, 0) : -1);
@@ -273,11 +285,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // no copy into this CTA's shared memory may still be in flight at exit
         asm volatile("cp.async.wait_all;" ::: "memory");
         if (lw == 0 && lane == 0 && last_q >= 0) drain_wait(q_full, last_q & 1);
-      } else {
-        // ---------------- MMA issuer (warp 7)
+      } else if (warp == kQkWarp) {
+        // ---------------- QK issuer (warp 6): S^T = K_blk . Q_t^T, chunk by chunk as rows land
         if (lane == 0) {
             constexpr uint32_t idesc_qk = idesc_bf16(128, 64, false, false);
-            constexpr uint32_t idesc_pv = idesc_bf16(128, 64, true, true);
             int tok = 0, g = 0;
             bool ok = true;
             for (int i = blockIdx.x; i < p.T && ok; i += gridDim.x, ++tok) {
@@ -285,25 +296,47 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 if (!(ok = mbar_wait(q_full, tok & 1, abort_flag, p.status))) break;
                 tc_fence_after();
                 for (int b = 0; b < x.nb && ok; ++b, ++g) {
+                    // S^T is single-buffered: the softmax of the previous block must have read it
+                    if (g > 0 && !(ok = mbar_wait(p_full, (g - 1) & 1, abort_flag, p.status))) break;
 #pragma unroll 1
-                    for (int c = 0; c < 8; ++c) {
-                        if (!(ok = mbar_wait(&kv_full[c], g & 1, abort_flag, p.status))) break;
+                    for (int m = 0; m < 4; ++m) {
+                        // one wait per chunk pair: a wait stalls this warp's MMA issue
+                        if (!(ok = mbar_wait(&kv_full[m], g & 1, abort_flag, p.status))) break;
                         // rows landed through the generic proxy; the MMA reads via the async proxy
                         fence_proxy_async_smem();
                         tc_fence_after();
-                        const uint64_t ad = desc_sw128(smem_u32(sKV + c * 16384), 16, 1024);
-                        const uint64_t bd = desc_sw128(smem_u32(sQ + c * 8192), 16, 1024);
 #pragma unroll
-                        for (int kk = 0; kk < 4; ++kk)
-                            mma_bf16(tmem + kSCol, ad + 2 * kk, bd + 2 * kk, idesc_qk,
-                                     (c | kk) != 0);
+                        for (int h = 0; h < 2; ++h) {
+                            const int c = 2 * m + h;
+                            const uint64_t ad = desc_sw128(smem_u32(sKV + c * 16384), 16, 1024);
+                            const uint64_t bd = desc_sw128(smem_u32(sQ + c * 8192), 16, 1024);
+#pragma unroll
+                            for (int kk = 0; kk < 4; ++kk)
+                                mma_bf16(tmem + kSCol, ad + 2 * kk, bd + 2 * kk, idesc_qk,
+                                         (c | kk) != 0);
+                        }
                     }
                     if (!ok) break;
                     mma_commit(s_full);
                     if (b == x.nb - 1) mma_commit(q_free);
+                }
+            }
+            mma_commit(&drain[0]);
+            drain_wait(&drain[0], 0);
+        }
+      } else {
+        // ---------------- PV issuer (warp 7): O^T += V_blk^T . P^T, one d-tile at a time
+        if (lane == 0) {
+            constexpr uint32_t idesc_pv = idesc_bf16(128, 64, true, true);
+            int tok = 0, g = 0;
+            bool ok = true;
+            for (int i = blockIdx.x; i < p.T && ok; i += gridDim.x, ++tok) {
+                const TokenInfo x = token_info(p, i);
+                for (int b = 0; b < x.nb && ok; ++b, ++g) {
                     if (!(ok = mbar_wait(p_full, g & 1, abort_flag, p.status))) break;
                     tc_fence_after();
                     if (b == 0 && tok > 0) {
+                        // the epilogue of the previous token must have read O^T
                         if (!(ok = mbar_wait(o_free, (tok - 1) & 1, abort_flag, p.status))) break;
                         tc_fence_after();
                     }
@@ -318,11 +351,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         }
                         mma_commit(&kv_free[m]);
                     }
+                    mma_commit(pv_done);
                     if (b == x.nb - 1) mma_commit(o_full);
                 }
             }
-            mma_commit(drain);
-            drain_wait(drain, 0);
+            mma_commit(&drain[1]);
+            drain_wait(&drain[1], 0);
         }
       }
     } else {
@@ -354,7 +388,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         pos < x.nsel ? __ldg(&p.sel[static_cast<int64_t>(i) * p.k + pos]) : -1;
                     valid = j >= 0 && j < x.nv;
                 }
-                const bool live = mbar_wait(s_full, g & 1, abort_flag, p.status);
+                // S^T of this block is ready; the PV of the previous block (issued by
+                // another warp) must be done with P and O^T before they change
+                bool live = mbar_wait(s_full, g & 1, abort_flag, p.status);
+                if (g > 0) live = mbar_wait(pv_done, (g - 1) & 1, abort_flag, p.status) && live;
                 tc_fence_after();
                 uint32_t sa[32];
                 if (live) {
@@ -512,7 +549,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         if (st == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     }
     __syncthreads();
-    if (warp == kMmaWarp) {
+    if (warp == kPvWarp) {
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, 512);
