@@ -118,19 +118,25 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
-// OR of `pred` over the 256 softmax threads (named barrier 1).
-__device__ __forceinline__ bool vote_any_soft(bool pred) {
+// The softmax warps form two groups of four, one per half of the heads (named
+// barriers 1 and 2, 128 threads each); barrier 3 spans all 256 softmax threads.
+// OR of `pred` over the 128 threads of head group hh.
+__device__ __forceinline__ bool vote_any_group(bool pred, int hh) {
     uint32_t r;
     asm volatile(
-        "{\n .reg .pred p, q;\n setp.ne.b32 p, %1, 0;\n bar.red.or.pred q, 1, 256, p;\n"
+        "{\n .reg .pred p, q;\n setp.ne.b32 p, %1, 0;\n bar.red.or.pred q, %2, 128, p;\n"
         " selp.b32 %0, 1, 0, q;\n}\n"
         : "=r"(r)
-        : "r"(static_cast<uint32_t>(pred))
+        : "r"(static_cast<uint32_t>(pred)), "r"(1 + hh)
         : "memory");
     return r != 0;
 }
 
-__device__ __forceinline__ void bar_soft() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+__device__ __forceinline__ void bar_group(int hh) {
+    asm volatile("bar.sync %0, 128;" ::"r"(1 + hh) : "memory");
+}
+
+__device__ __forceinline__ void bar_soft() { asm volatile("bar.sync 3, 256;" ::: "memory"); }
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
@@ -376,8 +382,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             float l[32];
 #pragma unroll
             for (int h = 0; h < 32; ++h) l[h] = 0.0f;
-            if (st < 64) sM[cur * 64 + st] = -INFINITY;
-            bar_soft();
+            if (sp == 0) sM[cur * 64 + hb + lane] = -INFINITY;
+            bar_group(hh);
             for (int b = 0; b < x.nb; ++b, ++g) {
                 bool valid;
                 if (b < x.nwb) {
@@ -399,19 +405,24 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     tmem_wait_ld();
                 }
                 valid = valid && live;
-                bool exceed = false;
+                // x = scale*log2e*logit - running max, once per (key, head); the same
+                // values decide the rescale and feed exp2
+                float xv[32];
+                float xmax = -INFINITY;
                 {
                     const float *m_now = sM + cur * 64 + hb;
 #pragma unroll
                     for (int h = 0; h < 32; h += 4) {
                         const float4 m4 = *reinterpret_cast<const float4 *>(&m_now[h]);
-                        exceed |= valid && fmaf(__uint_as_float(sa[h]), p.c, -m4.x) > kRescale;
-                        exceed |= valid && fmaf(__uint_as_float(sa[h + 1]), p.c, -m4.y) > kRescale;
-                        exceed |= valid && fmaf(__uint_as_float(sa[h + 2]), p.c, -m4.z) > kRescale;
-                        exceed |= valid && fmaf(__uint_as_float(sa[h + 3]), p.c, -m4.w) > kRescale;
+                        xv[h] = fmaf(__uint_as_float(sa[h]), p.c, -m4.x);
+                        xv[h + 1] = fmaf(__uint_as_float(sa[h + 1]), p.c, -m4.y);
+                        xv[h + 2] = fmaf(__uint_as_float(sa[h + 2]), p.c, -m4.z);
+                        xv[h + 3] = fmaf(__uint_as_float(sa[h + 3]), p.c, -m4.w);
                     }
+#pragma unroll
+                    for (int h = 0; h < 32; ++h) xmax = fmaxf(xmax, xv[h]);
                 }
-                if (vote_any_soft(exceed)) {
+                if (vote_any_group(valid && xmax > kRescale, hh)) {
                     // exact block maxima -> new running max, then rescale sums and O^T
 #pragma unroll
                     for (int h = 0; h < 32; ++h) {
@@ -419,19 +430,24 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                             redux_max(valid ? __uint_as_float(sa[h]) * p.c : -INFINITY);
                         if (lane == h) sRed[sp * 64 + hb + h] = wm;
                     }
-                    bar_soft();
-                    if (st < 64) {
-                        const float bm = fmaxf(fmaxf(sRed[st], sRed[64 + st]),
-                                               fmaxf(sRed[128 + st], sRed[192 + st]));
-                        const float m_old = sM[cur * 64 + st];
+                    bar_group(hh);
+                    if (sp == 0) {
+                        const int hd = hb + lane;
+                        const float bm = fmaxf(fmaxf(sRed[hd], sRed[64 + hd]),
+                                               fmaxf(sRed[128 + hd], sRed[192 + hd]));
+                        const float m_old = sM[cur * 64 + hd];
                         const float m_new = fmaxf(m_old, bm);
-                        sM[(cur ^ 1) * 64 + st] = m_new;
-                        sAlpha[st] = ex2(m_old - m_new);
+                        sM[(cur ^ 1) * 64 + hd] = m_new;
+                        sAlpha[hd] = ex2(m_old - m_new);
                     }
-                    bar_soft();
+                    bar_group(hh);
                     cur ^= 1;
+                    const float *m_now = sM + cur * 64 + hb;
 #pragma unroll
-                    for (int h = 0; h < 32; ++h) l[h] *= sAlpha[hb + h];
+                    for (int h = 0; h < 32; ++h) {
+                        l[h] *= sAlpha[hb + h];
+                        xv[h] = fmaf(__uint_as_float(sa[h]), p.c, -m_now[h]);
+                    }
                     if (b > 0 && live) {
 #pragma unroll 1
                         for (int m = 0; m < 4; ++m) {
@@ -449,27 +465,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 }
                 // this thread's 32 heads of the P^T row for key kl: 4 swizzled 16-byte pieces
                 {
-                    const float *m_use = sM + cur * 64 + hb;
+                    float pr[32];
+#pragma unroll
+                    for (int h = 0; h < 32; ++h) pr[h] = valid ? ex2(xv[h]) : 0.0f;
+#pragma unroll
+                    for (int h = 0; h < 32; ++h) l[h] += pr[h];
                     uint8_t *prow = sP + kl * 128;
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
                         uint32_t pk[4];
 #pragma unroll
-                        for (int h2 = 0; h2 < 8; h2 += 4) {
-                            const int h = 8 * q + h2;
-                            const float4 m4 = *reinterpret_cast<const float4 *>(&m_use[h]);
-                            const float mm[4] = {m4.x, m4.y, m4.z, m4.w};
-                            float pr[4];
-#pragma unroll
-                            for (int e = 0; e < 4; ++e) {
-                                pr[e] = valid ? ex2(fmaf(__uint_as_float(sa[h + e]), p.c, -mm[e]))
-                                              : 0.0f;
-                                l[h + e] += pr[e];
-                            }
-                            const __nv_bfloat162 v0 = __floats2bfloat162_rn(pr[0], pr[1]);
-                            const __nv_bfloat162 v1 = __floats2bfloat162_rn(pr[2], pr[3]);
-                            pk[h2 / 2] = *reinterpret_cast<const uint32_t *>(&v0);
-                            pk[h2 / 2 + 1] = *reinterpret_cast<const uint32_t *>(&v1);
+                        for (int e = 0; e < 4; ++e) {
+                            const __nv_bfloat162 v =
+                                __floats2bfloat162_rn(pr[8 * q + 2 * e], pr[8 * q + 2 * e + 1]);
+                            pk[e] = *reinterpret_cast<const uint32_t *>(&v);
                         }
                         *reinterpret_cast<uint4 *>(prow + (((4 * hh + q) ^ (kl & 7)) << 4)) =
                             make_uint4(pk[0], pk[1], pk[2], pk[3]);
