@@ -187,7 +187,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     uint64_t *o_full = bars + 16;
     uint64_t *o_free = bars + 17;
     uint64_t *drain = bars + 18;    // [2] one per issuing warp
-    uint64_t *pv_done = bars + 20;  // PV of a block complete (P and O^T free again)
+
     uint32_t *tmem_holder = reinterpret_cast<uint32_t *>(bars + 21);
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
 
@@ -197,13 +197,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         mbar_init(q_free, 1);
         for (int m = 0; m < 4; ++m) mbar_init(&kv_full[m], 32 * kLoadWarps);  // noinc arrivals
         for (int m = 0; m < 4; ++m) mbar_init(&kv_free[m], 1);
-        mbar_init(s_full, 1);
+        // a block's S^T is ready once its QK is done (QK warp) and the previous
+        // block's PV no longer reads P or writes O^T (PV warp)
+        mbar_init(s_full, 2);
         mbar_init(p_full, kSoftThreads);
         mbar_init(o_full, 1);
         mbar_init(o_free, 8);
         mbar_init(&drain[0], 1);
         mbar_init(&drain[1], 1);
-        mbar_init(pv_done, 1);
         *abort_flag = 0;
         fence_barrier_init();
     }
@@ -295,6 +296,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // ---------------- QK issuer (warp 6): S^T = K_blk . Q_t^T, chunk by chunk as rows land
         if (lane == 0) {
             constexpr uint32_t idesc_qk = idesc_bf16(128, 64, false, false);
+            const uint64_t ad0 = desc_sw128(smem_u32(sKV), 16, 1024);
+            const uint64_t bd0 = desc_sw128(smem_u32(sQ), 16, 1024);
             int tok = 0, g = 0;
             bool ok = true;
             for (int i = blockIdx.x; i < p.T && ok; i += gridDim.x, ++tok) {
@@ -311,16 +314,15 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         // rows landed through the generic proxy; the MMA reads via the async proxy
                         fence_proxy_async_smem();
                         tc_fence_after();
+                        const uint64_t ad = ad0 + ((2 * m * 16384) >> 4);
+                        const uint64_t bd = bd0 + ((2 * m * 8192) >> 4);
 #pragma unroll
-                        for (int h = 0; h < 2; ++h) {
-                            const int c = 2 * m + h;
-                            const uint64_t ad = desc_sw128(smem_u32(sKV + c * 16384), 16, 1024);
-                            const uint64_t bd = desc_sw128(smem_u32(sQ + c * 8192), 16, 1024);
+                        for (int h = 0; h < 2; ++h)
 #pragma unroll
                             for (int kk = 0; kk < 4; ++kk)
-                                mma_bf16(tmem + kSCol, ad + 2 * kk, bd + 2 * kk, idesc_qk,
-                                         (c | kk) != 0);
-                        }
+                                mma_bf16(tmem + kSCol, ad + ((h * 16384) >> 4) + 2 * kk,
+                                         bd + ((h * 8192) >> 4) + 2 * kk, idesc_qk,
+                                         (m | h | kk) != 0);
                     }
                     if (!ok) break;
                     mma_commit(s_full);
@@ -334,8 +336,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // ---------------- PV issuer (warp 7): O^T += V_blk^T . P^T, one d-tile at a time
         if (lane == 0) {
             constexpr uint32_t idesc_pv = idesc_bf16(128, 64, true, true);
+            const uint64_t ad0 = desc_sw128(smem_u32(sKV), 16384, 1024);
+            const uint64_t bd0 = desc_sw128(smem_u32(sP), 8192, 1024);
             int tok = 0, g = 0;
             bool ok = true;
+            mbar_arrive(s_full);  // no PV precedes the first block
             for (int i = blockIdx.x; i < p.T && ok; i += gridDim.x, ++tok) {
                 const TokenInfo x = token_info(p, i);
                 for (int b = 0; b < x.nb && ok; ++b, ++g) {
@@ -346,18 +351,16 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         if (!(ok = mbar_wait(o_free, (tok - 1) & 1, abort_flag, p.status))) break;
                         tc_fence_after();
                     }
+                    const uint32_t acc0 = b > 0;
 #pragma unroll 1
                     for (int m = 0; m < 4; ++m) {
 #pragma unroll
-                        for (int kk = 0; kk < 8; ++kk) {
-                            const uint64_t ad = desc_sw128(
-                                smem_u32(sKV + 2 * m * 16384 + kk * 2048), 16384, 1024);
-                            const uint64_t bd = desc_sw128(smem_u32(sP + kk * 2048), 8192, 1024);
-                            mma_bf16(tmem + kOCol + 64 * m, ad, bd, idesc_pv, (b > 0 || kk > 0));
-                        }
+                        for (int kk = 0; kk < 8; ++kk)
+                            mma_bf16(tmem + kOCol + 64 * m, ad0 + ((2 * m * 16384 + kk * 2048) >> 4),
+                                     bd0 + ((kk * 2048) >> 4), idesc_pv, kk > 0 ? 1u : acc0);
                         mma_commit(&kv_free[m]);
                     }
-                    mma_commit(pv_done);
+                    mma_commit(s_full);
                     if (b == x.nb - 1) mma_commit(o_full);
                 }
             }
@@ -394,10 +397,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         pos < x.nsel ? __ldg(&p.sel[static_cast<int64_t>(i) * p.k + pos]) : -1;
                     valid = j >= 0 && j < x.nv;
                 }
-                // S^T of this block is ready; the PV of the previous block (issued by
-                // another warp) must be done with P and O^T before they change
-                bool live = mbar_wait(s_full, g & 1, abort_flag, p.status);
-                if (g > 0) live = mbar_wait(pv_done, (g - 1) & 1, abort_flag, p.status) && live;
+                // S^T of this block is ready and the previous block's PV is done with P
+                // and O^T
+                const bool live = mbar_wait(s_full, g & 1, abort_flag, p.status);
                 tc_fence_after();
                 uint32_t sa[32];
                 if (live) {
@@ -419,8 +421,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         xv[h + 2] = fmaf(__uint_as_float(sa[h + 2]), p.c, -m4.z);
                         xv[h + 3] = fmaf(__uint_as_float(sa[h + 3]), p.c, -m4.w);
                     }
+                    float t16[16];
 #pragma unroll
-                    for (int h = 0; h < 32; ++h) xmax = fmaxf(xmax, xv[h]);
+                    for (int h = 0; h < 16; ++h) t16[h] = fmaxf(xv[h], xv[h + 16]);
+#pragma unroll
+                    for (int w = 8; w >= 1; w >>= 1)
+#pragma unroll
+                        for (int h = 0; h < w; ++h) t16[h] = fmaxf(t16[h], t16[h + w]);
+                    xmax = t16[0];
                 }
                 if (vote_any_group(valid && xmax > kRescale, hh)) {
                     // exact block maxima -> new running max, then rescale sums and O^T
