@@ -156,6 +156,27 @@ __device__ __forceinline__ void tma_store_2d(const CUtensorMap *tm, const void *
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
 
+// tcgen05.mma / tcgen05.commit executed by every lane of a converged warp but
+// issued only where `issue` is non-zero (one lane): the warp stays converged,
+// so the operand descriptors can stay in uniform registers.
+__device__ __forceinline__ void mma_bf16_if(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
+                                            uint32_t idesc, uint32_t accumulate, uint32_t issue) {
+    asm volatile(
+        "{\n .reg .pred p, q;\n setp.ne.b32 p, %4, 0;\n setp.ne.b32 q, %5, 0;\n"
+        " @q tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(issue)
+        : "memory");
+}
+
+__device__ __forceinline__ void mma_commit_if(uint64_t *bar, uint32_t issue) {
+    asm volatile(
+        "{\n .reg .pred q;\n setp.ne.b32 q, %1, 0;\n"
+        " @q tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n}\n" ::"r"(
+            smem_u32(bar)),
+        "r"(issue)
+        : "memory");
+}
+
 __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
     const uint32_t b = smem_u32(bar);
     const long long t0 = clock64();
@@ -293,80 +314,86 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         asm volatile("cp.async.wait_all;" ::: "memory");
         if (lw == 0 && lane == 0 && last_q >= 0) drain_wait(q_full, last_q & 1);
       } else if (warp == kQkWarp) {
-        // ---------------- QK issuer (warp 6): S^T = K_blk . Q_t^T, chunk by chunk as rows land
-        if (lane == 0) {
-            constexpr uint32_t idesc_qk = idesc_bf16(128, 64, false, false);
-            const uint64_t ad0 = desc_sw128(smem_u32(sKV), 16, 1024);
-            const uint64_t bd0 = desc_sw128(smem_u32(sQ), 16, 1024);
-            int tok = 0, g = 0;
-            bool ok = true;
-            for (int i = blockIdx.x; i < p.T && ok; i += gridDim.x, ++tok) {
-                const TokenInfo x = token_info(p, i);
-                if (!(ok = mbar_wait(q_full, tok & 1, abort_flag, p.status))) break;
-                tc_fence_after();
-                for (int b = 0; b < x.nb && ok; ++b, ++g) {
-                    // S^T is single-buffered: the softmax of the previous block must have read it
-                    if (g > 0 && !(ok = mbar_wait(p_full, (g - 1) & 1, abort_flag, p.status))) break;
+        // ---------------- QK issuer (warp 6): S^T = K_blk . Q_t^T, chunk pair by chunk pair
+        // as rows land. The whole warp runs the loop (descriptors stay warp-uniform) and
+        // lane 0 issues: a lone diverged lane issues MMAs markedly slower.
+        const uint32_t leader = lane == 0;
+        constexpr uint32_t idesc_qk = idesc_bf16(128, 64, false, false);
+        const uint64_t ad0 = desc_sw128(smem_u32(sKV), 16, 1024);
+        const uint64_t bd0 = desc_sw128(smem_u32(sQ), 16, 1024);
+        int tok = 0, g = 0;
+        bool ok = true;
+        for (int i = blockIdx.x; i < p.T && ok; i += gridDim.x, ++tok) {
+            const TokenInfo x = token_info(p, i);
+            if (!(ok = mbar_wait(q_full, tok & 1, abort_flag, p.status))) break;
+            tc_fence_after();
+            for (int b = 0; b < x.nb && ok; ++b, ++g) {
+                // S^T is single-buffered: the softmax of the previous block must have read it
+                if (g > 0 && !(ok = mbar_wait(p_full, (g - 1) & 1, abort_flag, p.status))) break;
 #pragma unroll 1
-                    for (int m = 0; m < 4; ++m) {
-                        // one wait per chunk pair: a wait stalls this warp's MMA issue
-                        if (!(ok = mbar_wait(&kv_full[m], g & 1, abort_flag, p.status))) break;
-                        // rows landed through the generic proxy; the MMA reads via the async proxy
-                        fence_proxy_async_smem();
-                        tc_fence_after();
-                        const uint64_t ad = ad0 + ((2 * m * 16384) >> 4);
-                        const uint64_t bd = bd0 + ((2 * m * 8192) >> 4);
-#pragma unroll
-                        for (int h = 0; h < 2; ++h)
-#pragma unroll
-                            for (int kk = 0; kk < 4; ++kk)
-                                mma_bf16(tmem + kSCol, ad + ((h * 16384) >> 4) + 2 * kk,
-                                         bd + ((h * 8192) >> 4) + 2 * kk, idesc_qk,
-                                         (m | h | kk) != 0);
-                    }
-                    if (!ok) break;
-                    mma_commit(s_full);
-                    if (b == x.nb - 1) mma_commit(q_free);
-                }
-            }
-            mma_commit(&drain[0]);
-            drain_wait(&drain[0], 0);
-        }
-      } else {
-        // ---------------- PV issuer (warp 7): O^T += V_blk^T . P^T, one d-tile at a time
-        if (lane == 0) {
-            constexpr uint32_t idesc_pv = idesc_bf16(128, 64, true, true);
-            const uint64_t ad0 = desc_sw128(smem_u32(sKV), 16384, 1024);
-            const uint64_t bd0 = desc_sw128(smem_u32(sP), 8192, 1024);
-            int tok = 0, g = 0;
-            bool ok = true;
-            mbar_arrive(s_full);  // no PV precedes the first block
-            for (int i = blockIdx.x; i < p.T && ok; i += gridDim.x, ++tok) {
-                const TokenInfo x = token_info(p, i);
-                for (int b = 0; b < x.nb && ok; ++b, ++g) {
-                    if (!(ok = mbar_wait(p_full, g & 1, abort_flag, p.status))) break;
+                for (int m = 0; m < 4; ++m) {
+                    // one wait per chunk pair: a wait stalls this warp's MMA issue
+                    if (!(ok = mbar_wait(&kv_full[m], g & 1, abort_flag, p.status))) break;
+                    // rows landed through the generic proxy; the MMA reads via the async proxy
+                    fence_proxy_async_smem();
                     tc_fence_after();
-                    if (b == 0 && tok > 0) {
-                        // the epilogue of the previous token must have read O^T
-                        if (!(ok = mbar_wait(o_free, (tok - 1) & 1, abort_flag, p.status))) break;
-                        tc_fence_after();
-                    }
-                    const uint32_t acc0 = b > 0;
-#pragma unroll 1
-                    for (int m = 0; m < 4; ++m) {
+                    const uint64_t ad = ad0 + ((2 * m * 16384) >> 4);
+                    const uint64_t bd = bd0 + ((2 * m * 8192) >> 4);
 #pragma unroll
-                        for (int kk = 0; kk < 8; ++kk)
-                            mma_bf16(tmem + kOCol + 64 * m, ad0 + ((2 * m * 16384 + kk * 2048) >> 4),
-                                     bd0 + ((kk * 2048) >> 4), idesc_pv, kk > 0 ? 1u : acc0);
-                        mma_commit(&kv_free[m]);
-                    }
-                    mma_commit(s_full);
-                    if (b == x.nb - 1) mma_commit(o_full);
+                    for (int h = 0; h < 2; ++h)
+#pragma unroll
+                        for (int kk = 0; kk < 4; ++kk)
+                            mma_bf16_if(tmem + kSCol, ad + ((h * 16384) >> 4) + 2 * kk,
+                                        bd + ((h * 8192) >> 4) + 2 * kk, idesc_qk,
+                                        (m | h | kk) != 0, leader);
                 }
+                if (!ok) break;
+                mma_commit_if(s_full, leader);
+                if (b == x.nb - 1) mma_commit_if(q_free, leader);
             }
-            mma_commit(&drain[1]);
-            drain_wait(&drain[1], 0);
         }
+        mma_commit_if(&drain[0], leader);
+        if (leader) drain_wait(&drain[0], 0);
+        __syncwarp();
+      } else {
+        // ---------------- PV issuer (warp 7): O^T += V_blk^T . P^T, one d-tile at a time;
+        // whole warp in the loop, lane 0 issues
+        const uint32_t leader = lane == 0;
+        constexpr uint32_t idesc_pv = idesc_bf16(128, 64, true, true);
+        const uint64_t ad0 = desc_sw128(smem_u32(sKV), 16384, 1024);
+        const uint64_t bd0 = desc_sw128(smem_u32(sP), 8192, 1024);
+        int tok = 0, g = 0;
+        bool ok = true;
+        if (leader) mbar_arrive(s_full);  // no PV precedes the first block
+        __syncwarp();
+        for (int i = blockIdx.x; i < p.T && ok; i += gridDim.x, ++tok) {
+            const TokenInfo x = token_info(p, i);
+            for (int b = 0; b < x.nb && ok; ++b, ++g) {
+                if (!(ok = mbar_wait(p_full, g & 1, abort_flag, p.status))) break;
+                tc_fence_after();
+                if (b == 0 && tok > 0) {
+                    // the epilogue of the previous token must have read O^T
+                    if (!(ok = mbar_wait(o_free, (tok - 1) & 1, abort_flag, p.status))) break;
+                    tc_fence_after();
+                }
+                const uint32_t acc0 = b > 0;
+#pragma unroll 1
+                for (int m = 0; m < 4; ++m) {
+#pragma unroll
+                    for (int kk = 0; kk < 8; ++kk)
+                        mma_bf16_if(tmem + kOCol + 64 * m,
+                                    ad0 + ((2 * m * 16384 + kk * 2048) >> 4),
+                                    bd0 + ((kk * 2048) >> 4), idesc_pv, kk > 0 ? 1u : acc0,
+                                    leader);
+                    mma_commit_if(&kv_free[m], leader);
+                }
+                mma_commit_if(s_full, leader);
+                if (b == x.nb - 1) mma_commit_if(o_full, leader);
+            }
+        }
+        mma_commit_if(&drain[1], leader);
+        if (leader) drain_wait(&drain[1], 0);
+        __syncwarp();
       }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoft));
