@@ -7,8 +7,9 @@ function names. There is no CPU fallback: calls raise if the library is missing.
 """
 from .buildlib import build as _build_lib
 from ._binding import (DIM, HEADS, INDEX_DIM, INDEX_HEADS, RATIO, DsaError, PoolState,  # noqa: F401
-                       dsa_bounded_wait_selftest, dsa_index_score_topk,
+                       PrefillWorkspace, dsa_bounded_wait_selftest, dsa_index_score_topk,
                        dsa_index_score_topk_noalloc, dsa_pool_append, dsa_prefill_chunk,
+                       dsa_prefill_chunk_host,
                        dsa_score_scratch_bytes, dsa_strerror, dsa_window_sparse_attn, load)
 
 

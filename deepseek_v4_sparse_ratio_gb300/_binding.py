@@ -23,7 +23,7 @@ DSA_ERR_BOUNDS, DSA_ERR_RAW_RANGE = -9, -10
 
 EXPORTS = ("dsa_pool_append", "dsa_score_scratch_bytes", "dsa_index_score_topk",
            "dsa_window_sparse_attn", "dsa_prefill_chunk", "dsa_strerror",
-           "dsa_index_score_topk_noalloc", "dsa_bounded_wait_selftest")
+           "dsa_index_score_topk_noalloc", "dsa_bounded_wait_selftest", "dsa_prefill_chunk_host")
 DSA_STATIC_SCRATCH_BYTES = 16 << 20
 
 
@@ -39,6 +39,14 @@ class dsa_pool_state(ctypes.Structure):
                 ("cap", ctypes.c_int64), ("n_pooled_kv", ctypes.c_int64),
                 ("n_pooled_ik", ctypes.c_int64), ("n_tokens", ctypes.c_int64),
                 ("n_rem", ctypes.c_int32), ("ratio", ctypes.c_int32)]
+
+
+class dsa_prefill_workspace(ctypes.Structure):
+    _fields_ = [("raw_kv", ctypes.c_void_p), ("raw_kv_rows", ctypes.c_int64),
+                ("raw_ik", ctypes.c_void_p), ("q_idx", ctypes.c_void_p), ("w", ctypes.c_void_p),
+                ("q", ctypes.c_void_p), ("sel", ctypes.c_void_p), ("out", ctypes.c_void_p),
+                ("scratch", ctypes.c_void_p), ("scratch_bytes", ctypes.c_size_t),
+                ("max_chunk", ctypes.c_int64), ("max_topk", ctypes.c_int32)]
 
 
 _lib = None
@@ -63,10 +71,14 @@ def load(path: str | None = None):
                                       ctypes.c_float, i64, P, sz, P, P, P, P]
     lib.dsa_index_score_topk_noalloc.argtypes = [P, P, P, i64, i64, i64, i32, i32, i64, P, P, P]
     lib.dsa_bounded_wait_selftest.argtypes = [i32, P, P]
+    lib.dsa_prefill_chunk_host.argtypes = [S, ctypes.POINTER(dsa_prefill_workspace), P, i64, i64,
+                                           P, P, P, P, i64, i64, i32, i32, ctypes.c_float, i64,
+                                           P, P, P, P, P]
     lib.dsa_strerror.argtypes = [ctypes.c_int]
     lib.dsa_strerror.restype = ctypes.c_char_p
     for f in ("dsa_pool_append", "dsa_index_score_topk", "dsa_window_sparse_attn",
-              "dsa_prefill_chunk", "dsa_index_score_topk_noalloc", "dsa_bounded_wait_selftest"):
+              "dsa_prefill_chunk", "dsa_index_score_topk_noalloc", "dsa_bounded_wait_selftest",
+              "dsa_prefill_chunk_host"):
         getattr(lib, f).restype = ctypes.c_int
     _lib = lib
     return lib
@@ -210,3 +222,39 @@ def dsa_prefill_chunk(state: PoolState, raw_kv, raw_start: int, raw_ik, q_idx, w
                                   window, scale, tile_rows, _p(scratch), _nbytes(scratch),
                                   _p(sel), _p(out), _p(dev_status), _s(stream))
     _check(rc, "dsa_prefill_chunk")
+
+
+class PrefillWorkspace:
+    """Device buffers for dsa_prefill_chunk_host (torch allocations, caller-owned)."""
+
+    def __init__(self, max_chunk: int, max_topk: int, raw_kv_rows: int, n_pooled_max: int,
+                 tile_rows: int, device="cuda"):
+        dev = torch.device(device)
+        self.raw_kv = torch.empty(raw_kv_rows, DIM, dtype=torch.bfloat16, device=dev)
+        self.raw_ik = torch.empty(max_chunk, INDEX_DIM, dtype=torch.bfloat16, device=dev)
+        self.q_idx = torch.empty(max_chunk, INDEX_HEADS, INDEX_DIM, dtype=torch.bfloat16,
+                                 device=dev)
+        self.w = torch.empty(max_chunk, INDEX_HEADS, dtype=torch.float32, device=dev)
+        self.q = torch.empty(max_chunk, HEADS, DIM, dtype=torch.bfloat16, device=dev)
+        self.sel = torch.empty(max_chunk, max_topk, dtype=torch.int32, device=dev)
+        self.out = torch.empty(max_chunk, HEADS, DIM, dtype=torch.bfloat16, device=dev)
+        nbytes = dsa_score_scratch_bytes(min(tile_rows, max_chunk), n_pooled_max)
+        self.scratch = torch.empty(max(nbytes // 4, 1), dtype=torch.float32, device=dev)
+        self.c = dsa_prefill_workspace(
+            self.raw_kv.data_ptr(), raw_kv_rows, self.raw_ik.data_ptr(), self.q_idx.data_ptr(),
+            self.w.data_ptr(), self.q.data_ptr(), self.sel.data_ptr(), self.out.data_ptr(),
+            self.scratch.data_ptr(), self.scratch.numel() * 4, max_chunk, max_topk)
+
+
+def dsa_prefill_chunk_host(state: "PoolState", ws: PrefillWorkspace, raw_kv_h, raw_start: int,
+                           raw_ik_h, q_idx_h, w_h, q_h, chunk: int, offset: int,
+                           index_topk: int, window: int, scale: float, tile_rows: int,
+                           sel_h, out_h, dev_status=None, stream=None,
+                           copy_stream=None) -> None:
+    """The whole path from host tensors (pinned for overlap) to host tensors."""
+    rc = load().dsa_prefill_chunk_host(
+        ctypes.byref(state.c), ctypes.byref(ws.c), _p(raw_kv_h), raw_start, raw_kv_h.shape[0],
+        _p(raw_ik_h), _p(q_idx_h), _p(w_h), _p(q_h), chunk, offset, index_topk, window, scale,
+        tile_rows, _p(sel_h), _p(out_h), _p(dev_status), _s(stream),
+        _s(copy_stream) if copy_stream is not None else _s(stream))
+    _check(rc, "dsa_prefill_chunk_host")

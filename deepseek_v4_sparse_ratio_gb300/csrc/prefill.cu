@@ -1,6 +1,8 @@
 // The whole path for one chunk: pool/append, score + top-k (or the skip path),
 // window + selected attention, enqueued in order on one stream with every
-// argument checked before the first launch.
+// argument checked before the first launch; and the same path from host
+// buffers, with the host<->device copies overlapped with the kernels on a
+// second stream.
 //
 // "perf(deepseek_v4): faster exact DeepSeek-V4 prefill", Summary (one prefill
 // step per chunk; the compressor runs in every step) and "[Discussion] Tile
@@ -21,13 +23,15 @@ int check_attention(const void *q, const void *raw_kv, int64_t raw_start, int64_
                     const void *out);
 }  // namespace dsa
 
-extern "C" int dsa_prefill_chunk(dsa_pool_state *st, const void *raw_kv, int64_t raw_start,
-                                 int64_t raw_rows, const void *raw_ik, const void *q_idx,
-                                 const float *w, const void *q, int64_t chunk, int64_t offset,
-                                 int32_t index_topk, int32_t window, float scale,
-                                 int64_t tile_rows, void *scratch, size_t scratch_bytes,
-                                 int32_t *sel, void *out, int32_t *dev_status, void *stream) {
-    using namespace dsa;
+namespace dsa {
+namespace {
+
+// Every argument of one chunk's path, checked before anything is enqueued.
+int check_prefill(const dsa_pool_state *st, const void *raw_kv, int64_t raw_start,
+                  int64_t raw_rows, const void *raw_ik, const void *q_idx, const float *w,
+                  const void *q, int64_t chunk, int64_t offset, int32_t index_topk,
+                  int32_t window, float scale, int64_t tile_rows, const void *scratch,
+                  size_t scratch_bytes, const int32_t *sel, const void *out) {
     if (!st || !raw_kv || !raw_ik || chunk <= 0 || offset < 0) return DSA_ERR_ARG;
     if (!st->pooled_kv || !st->pooled_ik || !st->rem_kv || !st->rem_ik) return DSA_ERR_ARG;
     if (!aligned16(raw_ik) || !aligned16(st->pooled_kv) || !aligned16(st->pooled_ik) ||
@@ -40,27 +44,142 @@ extern "C" int dsa_prefill_chunk(dsa_pool_state *st, const void *raw_kv, int64_t
         st->n_pooled_kv * ratio + st->n_rem != st->n_tokens)
         return DSA_ERR_ARG;
     if (offset != st->n_tokens) return DSA_ERR_OFFSET;
-    const int64_t end = offset + chunk;
-    const int64_t n = end / ratio;
+    const int64_t n = (offset + chunk) / ratio;
     if (n > st->cap) return DSA_ERR_CAPACITY;
     int rc = check_score_topk(q_idx, w, st->pooled_ik, n, chunk, offset, ratio, index_topk,
                               tile_rows, scratch, scratch_bytes, sel);
     if (rc != DSA_OK) return rc;
-    rc = check_attention(q, raw_kv, raw_start, raw_rows, st->pooled_kv, n, sel, index_topk, chunk,
-                         offset, ratio, window, scale, out);
-    if (rc != DSA_OK) return rc;
+    return check_attention(q, raw_kv, raw_start, raw_rows, st->pooled_kv, n, sel, index_topk,
+                           chunk, offset, ratio, window, scale, out);
+}
 
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
+// Pool/append + score/top-k for one chunk on stream s (arguments already checked);
+// advances the host-side state.
+int enqueue_pool_and_select(dsa_pool_state *st, const void *raw_kv, int64_t raw_start,
+                            const void *raw_ik, const void *q_idx, const float *w,
+                            int64_t chunk, int64_t offset, int32_t index_topk,
+                            int64_t tile_rows, void *scratch, int32_t *sel, int32_t *status,
+                            cudaStream_t s) {
+    const int32_t ratio = st->ratio;
+    const int64_t end = offset + chunk;
+    const int64_t n = end / ratio;
     const void *chunk_kv =
         static_cast<const uint8_t *>(raw_kv) + (offset - raw_start) * int64_t{kD} * 2;
-    rc = launch_pool_append(*st, chunk_kv, raw_ik, chunk, offset, s);
+    int rc = launch_pool_append(*st, chunk_kv, raw_ik, chunk, offset, s);
     if (rc != DSA_OK) return rc;
     st->n_pooled_kv = st->n_pooled_ik = n;
     st->n_tokens = end;
     st->n_rem = static_cast<int32_t>(end % ratio);
-    rc = run_score_topk(q_idx, w, st->pooled_ik, n, chunk, offset, ratio, index_topk, tile_rows,
-                        scratch, sel, dev_status, s);
+    return run_score_topk(q_idx, w, st->pooled_ik, n, chunk, offset, ratio, index_topk,
+                          tile_rows, scratch, sel, status, s);
+}
+
+}  // namespace
+}  // namespace dsa
+
+extern "C" int dsa_prefill_chunk(dsa_pool_state *st, const void *raw_kv, int64_t raw_start,
+                                 int64_t raw_rows, const void *raw_ik, const void *q_idx,
+                                 const float *w, const void *q, int64_t chunk, int64_t offset,
+                                 int32_t index_topk, int32_t window, float scale,
+                                 int64_t tile_rows, void *scratch, size_t scratch_bytes,
+                                 int32_t *sel, void *out, int32_t *dev_status, void *stream) {
+    using namespace dsa;
+    int rc = check_prefill(st, raw_kv, raw_start, raw_rows, raw_ik, q_idx, w, q, chunk, offset,
+                           index_topk, window, scale, tile_rows, scratch, scratch_bytes, sel, out);
     if (rc != DSA_OK) return rc;
-    return launch_attention(q, raw_kv, raw_start, raw_rows, st->pooled_kv, n, sel, index_topk,
-                            chunk, offset, ratio, window, scale, out, dev_status, s);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    rc = enqueue_pool_and_select(st, raw_kv, raw_start, raw_ik, q_idx, w, chunk, offset,
+                                 index_topk, tile_rows, scratch, sel, dev_status, s);
+    if (rc != DSA_OK) return rc;
+    return launch_attention(q, raw_kv, raw_start, raw_rows, st->pooled_kv, st->n_pooled_kv, sel,
+                            index_topk, chunk, offset, st->ratio, window, scale, out, dev_status,
+                            s);
+}
+
+namespace {
+
+struct Events {
+    cudaEvent_t e[8] = {};
+    int n = 0;
+    ~Events() {
+        for (int i = 0; i < n; ++i) cudaEventDestroy(e[i]);  // released once complete
+    }
+    cudaEvent_t make() {
+        if (n == 8 || cudaEventCreateWithFlags(&e[n], cudaEventDisableTiming) != cudaSuccess)
+            return nullptr;
+        return e[n++];
+    }
+};
+
+}  // namespace
+
+extern "C" int dsa_prefill_chunk_host(dsa_pool_state *st, const dsa_prefill_workspace *ws,
+                                      const void *raw_kv_h, int64_t raw_start, int64_t raw_rows,
+                                      const void *raw_ik_h, const void *q_idx_h, const float *w_h,
+                                      const void *q_h, int64_t chunk, int64_t offset,
+                                      int32_t index_topk, int32_t window, float scale,
+                                      int64_t tile_rows, int32_t *sel_h, void *out_h,
+                                      int32_t *dev_status, void *stream, void *copy_stream) {
+    using namespace dsa;
+    if (!ws || !raw_kv_h || !raw_ik_h || !q_idx_h || !w_h || !q_h || !sel_h || !out_h)
+        return DSA_ERR_ARG;
+    if (chunk > ws->max_chunk || index_topk > ws->max_topk || raw_rows > ws->raw_kv_rows)
+        return DSA_ERR_CAPACITY;
+    int rc = check_prefill(st, ws->raw_kv, raw_start, raw_rows, ws->raw_ik, ws->q_idx, ws->w,
+                           ws->q, chunk, offset, index_topk, window, scale, tile_rows,
+                           ws->scratch, ws->scratch_bytes, ws->sel, ws->out);
+    if (rc != DSA_OK) return rc;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaStream_t c = static_cast<cudaStream_t>(copy_stream);
+    const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
+    const size_t q_row = size_t{kH} * kD * 2;  // bytes of one query row (all heads)
+    Events ev;
+    cudaEvent_t in_done = ev.make(), q_done = ev.make(), sel_done = ev.make(), all_done = ev.make();
+    if (!in_done || !q_done || !sel_done || !all_done) return DSA_ERR_CUDA;
+    bool ok = true;
+    // inputs of pooling and the indexer on the compute stream; the query rows follow on
+    // the copy stream and land while pooling and the indexer run
+    ok = ok && cudaMemcpyAsync(ws->raw_kv, raw_kv_h, size_t(raw_rows) * kD * 2, h2d, s) == cudaSuccess;
+    ok = ok && cudaMemcpyAsync(ws->raw_ik, raw_ik_h, size_t(chunk) * kDI * 2, h2d, s) == cudaSuccess;
+    ok = ok && cudaMemcpyAsync(ws->q_idx, q_idx_h, size_t(chunk) * kHI * kDI * 2, h2d, s) == cudaSuccess;
+    ok = ok && cudaMemcpyAsync(ws->w, w_h, size_t(chunk) * kHI * 4, h2d, s) == cudaSuccess;
+    ok = ok && cudaEventRecord(in_done, s) == cudaSuccess;
+    ok = ok && cudaStreamWaitEvent(c, in_done, 0) == cudaSuccess;
+    ok = ok && cudaMemcpyAsync(ws->q, q_h, size_t(chunk) * q_row, h2d, c) == cudaSuccess;
+    ok = ok && cudaEventRecord(q_done, c) == cudaSuccess;
+    if (!ok) return DSA_ERR_CUDA;
+
+    rc = enqueue_pool_and_select(st, ws->raw_kv, raw_start, ws->raw_ik, ws->q_idx, ws->w, chunk,
+                                 offset, index_topk, tile_rows, ws->scratch, ws->sel, dev_status, s);
+    if (rc != DSA_OK) return rc;
+    ok = ok && cudaEventRecord(sel_done, s) == cudaSuccess;
+    ok = ok && cudaStreamWaitEvent(c, sel_done, 0) == cudaSuccess;
+    ok = ok && cudaMemcpyAsync(sel_h, ws->sel, size_t(chunk) * index_topk * 4, d2h, c) == cudaSuccess;
+    ok = ok && cudaStreamWaitEvent(s, q_done, 0) == cudaSuccess;
+    if (!ok) return DSA_ERR_CUDA;
+
+    // attention in row slices; each slice's output goes back while the next computes
+    const int slices = chunk >= 2048 ? 4 : (chunk >= 1024 ? 2 : 1);
+    const int64_t per = (chunk + slices - 1) / slices;
+    for (int64_t r0 = 0; r0 < chunk; r0 += per) {
+        const int64_t rows = chunk - r0 < per ? chunk - r0 : per;
+        rc = launch_attention(static_cast<const uint8_t *>(ws->q) + r0 * q_row, ws->raw_kv,
+                              raw_start, raw_rows, st->pooled_kv, st->n_pooled_kv,
+                              ws->sel + r0 * index_topk, index_topk, rows, offset + r0,
+                              st->ratio, window, scale,
+                              static_cast<uint8_t *>(ws->out) + r0 * q_row, dev_status, s);
+        if (rc != DSA_OK) return rc;
+        cudaEvent_t slice_done = ev.make();
+        if (!slice_done) return DSA_ERR_CUDA;
+        ok = ok && cudaEventRecord(slice_done, s) == cudaSuccess;
+        ok = ok && cudaStreamWaitEvent(c, slice_done, 0) == cudaSuccess;
+        ok = ok && cudaMemcpyAsync(static_cast<uint8_t *>(out_h) + r0 * q_row,
+                                   static_cast<const uint8_t *>(ws->out) + r0 * q_row,
+                                   size_t(rows) * q_row, d2h, c) == cudaSuccess;
+        if (!ok) return DSA_ERR_CUDA;
+    }
+    ok = ok && cudaEventRecord(all_done, c) == cudaSuccess;
+    ok = ok && cudaStreamWaitEvent(s, all_done, 0) == cudaSuccess;
+    return ok ? DSA_OK : DSA_ERR_CUDA;
 }

@@ -10,7 +10,8 @@
  *                              then per-row top-k, skipped when the pool fits;
  *   (d) dsa_window_sparse_attn exact attention over the raw sliding window plus
  *                              the selected pooled rows;
- *   dsa_prefill_chunk          the four steps for one chunk, in order.
+ *   dsa_prefill_chunk          the four steps for one chunk, in order;
+ *   dsa_prefill_chunk_host     the same from host buffers, copies overlapped.
  *
  * Shapes are fixed by the model: indexer heads H_I=64 of dim d_I=128, query
  * heads H=64, one shared KV row of dim D=512 (key and value for every head),
@@ -20,7 +21,8 @@
  *
  * Conventions for every call:
  *   - All tensor pointers are DEVICE pointers to row-major, densely packed
- *     arrays, 16-byte aligned. The library never allocates, frees or keeps a
+ *     arrays, 16-byte aligned (except the *_h arguments of
+ *     dsa_prefill_chunk_host, which are host pointers). The library never allocates, frees or keeps a
  *     pointer after the call returns; the caller owns all memory.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream). Work is
  *     enqueued asynchronously; host-side state (dsa_pool_state counters) is
@@ -212,6 +214,60 @@ int dsa_prefill_chunk(dsa_pool_state *st, const void *raw_kv, int64_t raw_start,
                       int32_t index_topk, int32_t window, float scale, int64_t tile_rows,
                       void *scratch, size_t scratch_bytes, int32_t *sel, void *out,
                       int32_t *dev_status, void *stream);
+
+/*
+ * Device buffers for dsa_prefill_chunk_host, allocated and owned by the
+ * caller (16-byte aligned device pointers). Capacities are in rows.
+ */
+typedef struct dsa_prefill_workspace {
+    void *raw_kv;          /* [raw_kv_rows, 512] bf16 */
+    int64_t raw_kv_rows;
+    void *raw_ik;          /* [max_chunk, 128] bf16 */
+    void *q_idx;           /* [max_chunk, 64, 128] bf16 */
+    float *w;              /* [max_chunk, 64] fp32 */
+    void *q;               /* [max_chunk, 64, 512] bf16 */
+    int32_t *sel;          /* [max_chunk, max_topk] int32 */
+    void *out;             /* [max_chunk, 64, 512] bf16 */
+    void *scratch;         /* score scratch, see dsa_score_scratch_bytes */
+    size_t scratch_bytes;
+    int64_t max_chunk;
+    int32_t max_topk;
+} dsa_prefill_workspace;
+
+/*
+ * dsa_prefill_chunk for inputs and outputs in HOST memory: copies the chunk's
+ * inputs to the workspace, runs the four steps and copies the selection and
+ * the output back, overlapping the copies with the kernels.
+ * The pages have no counterpart to this entry point: it is an addition of this
+ * library (their prefill step starts from device-resident activations).
+ *
+ *   raw_kv_h [raw_rows, 512], raw_ik_h [chunk, 128], q_idx_h [chunk, 64, 128],
+ *   w_h [chunk, 64] fp32, q_h [chunk, 64, 512]: host inputs with the meaning
+ *   they have in dsa_prefill_chunk; sel_h [chunk, index_topk] int32 and
+ *   out_h [chunk, 64, 512] bf16: host outputs. Pinned (page-locked) host
+ *   memory is needed for the copies to overlap; pageable memory works but
+ *   serializes them.
+ *   ws: device buffers; chunk <= ws->max_chunk, index_topk <= ws->max_topk,
+ *   raw_rows <= ws->raw_kv_rows, ws->scratch as for dsa_prefill_chunk.
+ *   stream: the compute stream; copy_stream: a second stream for the copies
+ *   that overlap compute (the query copy, the selection and output copies), or
+ *   the same stream to serialize everything. Ordering: the inputs are copied
+ *   on `stream`, the query rows on copy_stream while the pooling and indexer
+ *   run, the attention runs in up to four row slices and each slice's output
+ *   is copied back on copy_stream while the next slice computes. When `stream`
+ *   completes, every copy has completed and the host outputs are valid.
+ *   The host buffers must stay alive and unmodified until then.
+ * Errors: those of dsa_prefill_chunk; DSA_ERR_ARG for a null host pointer or
+ * workspace, DSA_ERR_CAPACITY when the chunk, index_topk or raw rows exceed
+ * the workspace; DSA_ERR_CUDA if an event, copy or launch fails (after the
+ * first enqueue the pool state has been advanced).
+ */
+int dsa_prefill_chunk_host(dsa_pool_state *st, const dsa_prefill_workspace *ws,
+                           const void *raw_kv_h, int64_t raw_start, int64_t raw_rows,
+                           const void *raw_ik_h, const void *q_idx_h, const float *w_h,
+                           const void *q_h, int64_t chunk, int64_t offset, int32_t index_topk,
+                           int32_t window, float scale, int64_t tile_rows, int32_t *sel_h,
+                           void *out_h, int32_t *dev_status, void *stream, void *copy_stream);
 
 /*
  * Library-held score scratch: the size of the device array that

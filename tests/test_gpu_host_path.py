@@ -1,0 +1,53 @@
+"""dsa_prefill_chunk_host: the whole path from pinned host buffers with the
+copies overlapped on a second stream must give exactly what the device path
+gives (same kernels, the attention only split into row slices), chunk after
+chunk, and leave the PoolingCache in the same state."""
+import math
+
+import pytest
+import torch
+
+from deepseek_v4_sparse_ratio_gb300 import _binding as B
+from deepseek_v4_sparse_ratio_gb300 import inputs
+from deepseek_v4_sparse_ratio_gb300.runner import DeviceWorkload
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.mark.parametrize("name,copy_stream", [("two_chunks_4098", True),
+                                              ("two_chunks_4098", False)])
+def test_host_path_equals_device_path(dsa, name, copy_stream):
+    wl = inputs.draw(inputs.workload(name))
+    dw = DeviceWorkload(wl, tile_rows=wl.tile_rows[0])
+    W = wl.window
+    raw_all = torch.cat([wl.t["prefix_win"], wl.t["raw_kv"]], 0).pin_memory()
+    raw_base = wl.off0 - wl.t["prefix_win"].shape[0]
+    tmax = max(wl.chunks)
+    ws = B.PrefillWorkspace(tmax, wl.index_topk, tmax + W - 1, wl.end // wl.ratio,
+                            wl.tile_rows[0])
+    st = B.PoolState(wl.end // wl.ratio, "cuda", wl.ratio)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    side = torch.cuda.Stream() if copy_stream else None
+    scale = 1.0 / math.sqrt(B.DIM)
+    for c, s, T, off in wl.chunk_bounds():
+        dw.run_chunk(c)
+        torch.cuda.synchronize()
+        dw.check_status()
+        r0 = max(0, off - W + 1) - raw_base
+        raw_h = raw_all[r0:off + T - raw_base]
+        pin = lambda t: t.contiguous().pin_memory()
+        sel_h = torch.empty(T, wl.index_topk, dtype=torch.int32).pin_memory()
+        out_h = torch.empty(T, B.HEADS, B.DIM, dtype=torch.bfloat16).pin_memory()
+        B.dsa_prefill_chunk_host(st, ws, raw_h, raw_base + r0, pin(wl.t["raw_ik"][s:s + T]),
+                                 pin(wl.t["q_idx"][s:s + T]), pin(wl.t["w"][s:s + T]),
+                                 pin(wl.t["q"][s:s + T]), T, off, wl.index_topk, W, scale,
+                                 wl.tile_rows[0], sel_h, out_h, status, None, side)
+        torch.cuda.current_stream().synchronize()
+        assert status.item() == 0
+        assert torch.equal(sel_h, dw.sel[:T].cpu())
+        assert torch.equal(out_h.view(torch.int16), dw.out[:T].cpu().view(torch.int16))
+        assert (st.n_pooled, st.n_tokens, st.n_rem) == \
+            (dw.state.n_pooled, dw.state.n_tokens, dw.state.n_rem)
+    n = st.n_pooled
+    assert torch.equal(st.pooled_kv[:n], dw.state.pooled_kv[:n])
+    assert torch.equal(st.pooled_ik[:n], dw.state.pooled_ik[:n])

@@ -121,3 +121,27 @@ def test_prefill_chunk_validates_everything_first(lib):
 
 def test_wait_selftest_rejects_null_status(lib):
     assert lib.dsa_bounded_wait_selftest(0, None, None) == B.DSA_ERR_ARG
+
+
+def test_host_prefill_rejects_before_any_copy(lib):
+    ws = B.dsa_prefill_workspace(FAKE, 200, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1 << 20,
+                                 100, 64)
+    st = B.dsa_pool_state(FAKE, FAKE, FAKE, FAKE, 1000, 0, 0, 0, 0, 4)
+    args = [FAKE, 0, 100, FAKE, FAKE, FAKE, FAKE, 100, 0, 64, 128, 0.05, 100, FAKE, FAKE, None,
+            None, None]
+    assert lib.dsa_prefill_chunk_host(ctypes.byref(st), None, *args) == B.DSA_ERR_ARG
+    bad = list(args)
+    bad[3] = None   # raw_ik_h
+    assert lib.dsa_prefill_chunk_host(ctypes.byref(st), ctypes.byref(ws), *bad) == B.DSA_ERR_ARG
+    big = list(args)
+    big[7] = 101    # chunk beyond the workspace
+    assert lib.dsa_prefill_chunk_host(ctypes.byref(st), ctypes.byref(ws), *big) == \
+        B.DSA_ERR_CAPACITY
+    big = list(args)
+    big[9] = 65     # index_topk beyond the workspace
+    assert lib.dsa_prefill_chunk_host(ctypes.byref(st), ctypes.byref(ws), *big) == \
+        B.DSA_ERR_CAPACITY
+    off = list(args)
+    off[8] = 4      # offset != tokens in the cache
+    assert lib.dsa_prefill_chunk_host(ctypes.byref(st), ctypes.byref(ws), *off) == \
+        B.DSA_ERR_OFFSET
