@@ -357,11 +357,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         __syncwarp();
       } else {
         // ---------------- PV issuer (warp 7): O^T += V_blk^T . P^T, one d-tile at a time;
-        // whole warp in the loop, lane 0 issues
+        // whole warp in the loop, lane 0 issues the 32 MMAs of a block in one straight run
         const uint32_t leader = lane == 0;
         constexpr uint32_t idesc_pv = idesc_bf16(128, 64, true, true);
-        const uint64_t ad0 = desc_sw128(smem_u32(sKV), 16384, 1024);
-        const uint64_t bd0 = desc_sw128(smem_u32(sP), 8192, 1024);
         int tok = 0, g = 0;
         bool ok = true;
         if (leader) mbar_arrive(s_full);  // no PV precedes the first block
@@ -377,16 +375,19 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     tc_fence_after();
                 }
                 const uint32_t acc0 = b > 0;
-#pragma unroll 1
-                for (int m = 0; m < 4; ++m) {
+                if (leader) {
 #pragma unroll
-                    for (int kk = 0; kk < 8; ++kk)
-                        mma_bf16_if(tmem + kOCol + 64 * m,
-                                    ad0 + ((2 * m * 16384 + kk * 2048) >> 4),
-                                    bd0 + ((kk * 2048) >> 4), idesc_pv, kk > 0 ? 1u : acc0,
-                                    leader);
-                    mma_commit_if(&kv_free[m], leader);
+                    for (int m = 0; m < 4; ++m) {
+#pragma unroll
+                        for (int kk = 0; kk < 8; ++kk)
+                            mma_bf16(tmem + kOCol + 64 * m,
+                                     desc_sw128(smem_u32(sKV + 2 * m * 16384 + kk * 2048), 16384, 1024),
+                                     desc_sw128(smem_u32(sP + kk * 2048), 8192, 1024), idesc_pv,
+                                     kk > 0 ? 1u : acc0);
+                        mma_commit(&kv_free[m]);
+                    }
                 }
+                __syncwarp();
                 mma_commit_if(s_full, leader);
                 if (b == x.nb - 1) mma_commit_if(o_full, leader);
             }
