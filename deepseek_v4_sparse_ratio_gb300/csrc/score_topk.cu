@@ -317,7 +317,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 constexpr int kTopkThreads = 256;
 constexpr int kTopkWarps = kTopkThreads / 32;
 constexpr int kBins = 2048;
-constexpr int kCandCap = 4096;
+constexpr int kCandCap = 2048;
 
 __device__ __forceinline__ uint32_t order_key(float f) {
     const uint32_t b = __float_as_uint(f);
@@ -375,43 +375,30 @@ __device__ __forceinline__ void find_bin(const uint32_t *hist, int nb, uint32_t 
     __syncthreads();
 }
 
-// Radix select over `count` order keys given by key_at(i), all of which share
-// their bits above bit `low_bits` (a prefix equal to that of `any_key`): the
-// key of the need-th largest element and how many elements equal to it are
-// kept. The low bits are resolved in 1-3 digits of 8 to 11 bits from the top;
-// a digit may reach into the common prefix, which only costs resolution it
-// does not need. Skipping the common prefix matters because the candidates of
-// one linear bin agree on their top bits, and a digit they all share would
-// send every candidate to the same histogram bin.
+// Radix select over `count` order keys given by key_at(i): the key of the
+// need-th largest element and how many elements equal to it are kept
+// (11/11/10-bit digits from the top).
 template <typename KeyAt>
 __device__ __forceinline__ void radix_select(KeyAt key_at, int64_t count, uint32_t need,
-                                             int low_bits, uint32_t any_key, uint32_t *hist,
-                                             uint32_t *warp_sums, uint32_t *s_bin,
+                                             uint32_t *hist, uint32_t *warp_sums, uint32_t *s_bin,
                                              uint32_t *s_above, uint32_t *thr_out,
                                              uint32_t *need_out) {
-    int tb = low_bits < 8 ? 8 : low_bits;
-    if (tb >= 12 && tb <= 15) tb = 16;
-    if (tb == 23) tb = 24;
-    const int passes = (tb + 10) / 11;
-    uint32_t prefix = tb == 32 ? 0u : any_key >> tb;
-    int rem = tb;
-    for (int pass = 0; pass < passes; ++pass) {
-        // near-equal digits, the first ones one bit larger
-        const int bits = tb / passes + (pass < tb % passes ? 1 : 0);
-        const int shift = rem - bits;
+    uint32_t prefix = 0;
+    for (int pass = 0; pass < 3; ++pass) {
+        const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+        const int bits = pass == 2 ? 10 : 11;
         const int nb = 1 << bits;
         for (int i = threadIdx.x; i < nb; i += kTopkThreads) hist[i] = 0;
         __syncthreads();
         for (int64_t j = threadIdx.x; j < count; j += kTopkThreads) {
             const uint32_t u = key_at(j);
-            if ((static_cast<uint64_t>(u) >> rem) == prefix)
+            if (pass == 0 || (u >> (shift + bits)) == prefix)
                 atomicAdd(&hist[(u >> shift) & (nb - 1)], 1u);
         }
         __syncthreads();
         find_bin(hist, nb, need, warp_sums, s_bin, s_above);
         prefix = (prefix << bits) | *s_bin;
         need -= *s_above;
-        rem = shift;
         __syncthreads();
     }
     *thr_out = prefix;
@@ -420,7 +407,7 @@ __device__ __forceinline__ void radix_select(KeyAt key_at, int64_t count, uint32
 
 // Eight loads of a warp-strided walk issued together (more bytes in flight per
 // thread: the passes are bound by load latency, not bandwidth).
-constexpr int kBatch = 16;
+constexpr int kBatch = 8;
 
 template <typename F>
 __device__ __forceinline__ void walk(const float *__restrict__ src, int64_t lo, int64_t hi, F f) {
@@ -440,217 +427,9 @@ __device__ __forceinline__ void walk(const float *__restrict__ src, int64_t lo, 
     }
 }
 
-// Sampled fast path for one row (L > k): a strided sample of the row puts a
-// lower bound under the k-th largest score with a wide margin; one pass over
-// the row collects every score at or above it; an exact radix select among
-// those gives the threshold, and the kept entries are written in index order.
-// Returns false, with every thread agreeing and shared state free for reuse,
-// when the bound turns out not to hold (fewer than k collected) or the
-// collection overflows: the caller then runs the exact multi-pass path. The
-// result never depends on the sample, only the time taken does.
-//
-// Order without sorting: each warp walks its own contiguous segment of the row
-// in order and reserves list space once per batch of 16 steps, so the list is
-// made of chunks that are ascending in index, and a warp's chunks (which it
-// records) are in its walking order; warps own ascending segments.
-constexpr int kMaxChunks = 128;  // per warp
-
-__device__ __noinline__ bool topk_sampled(const float *__restrict__ src, int64_t L, int32_t k,
-                                          int32_t *__restrict__ out, uint32_t *hist,
-                                          uint32_t *cand, int32_t *cand_j, uint32_t *warp_sums,
-                                          uint32_t *s_bin, uint32_t *s_above, uint32_t *s_cnt,
-                                          float *s_min, float *s_max, uint32_t *w_a,
-                                          uint32_t *w_b, uint32_t (*chunks)[kMaxChunks]) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    // about 128 sampled scores expected above the k-th largest
-    const int64_t want = min(L, max(int64_t{2048}, (128 * L + k - 1) / k));
-    const int64_t step = max(int64_t{1}, L / want);
-    const int64_t S = (L + step - 1) / step;
-    float smin = INFINITY, smax = -INFINITY;
-    for (int64_t i0 = threadIdx.x; i0 < S; i0 += 8 * kTopkThreads) {
-        float v[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int64_t i = i0 + e * kTopkThreads;
-            v[e] = i < S ? __ldg(src + i * step) : __ldg(src);
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            smin = fminf(smin, v[e]);
-            smax = fmaxf(smax, v[e]);
-        }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        smin = fminf(smin, __shfl_xor_sync(0xFFFFFFFFu, smin, o));
-        smax = fmaxf(smax, __shfl_xor_sync(0xFFFFFFFFu, smax, o));
-    }
-    if (lane == 0) {
-        s_min[warp] = smin;
-        s_max[warp] = smax;
-    }
-    for (int i = threadIdx.x; i < kBins; i += kTopkThreads) hist[i] = 0;
-    if (threadIdx.x == 0) *s_cnt = 0;
-    __syncthreads();
-    smin = s_min[0];
-    smax = s_max[0];
-#pragma unroll
-    for (int w = 1; w < kTopkWarps; ++w) {
-        smin = fminf(smin, s_min[w]);
-        smax = fmaxf(smax, s_max[w]);
-    }
-    if (!(smax > smin) || !isfinite(smax - smin)) return false;  // uniform: same for all
-    const float scale = static_cast<float>(kBins) / (smax - smin);
-    // monotone bin of any score (clamped below smin and above smax)
-    auto bin_of = [&](float v) {
-        const float x = (v - smin) * scale;
-        return x <= 0.0f ? 0 : (x >= static_cast<float>(kBins - 1) ? kBins - 1 : static_cast<int>(x));
-    };
-    for (int64_t i0 = threadIdx.x; i0 < S; i0 += 8 * kTopkThreads) {
-        float v[8];
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-            const int64_t i = i0 + e * kTopkThreads;
-            v[e] = i < S ? __ldg(src + i * step) : 0.0f;
-        }
-#pragma unroll
-        for (int e = 0; e < 8; ++e)
-            if (i0 + e * kTopkThreads < S) atomicAdd(&hist[bin_of(v[e])], 1u);
-    }
-    __syncthreads();
-    const double ks = static_cast<double>(k) * static_cast<double>(S) / static_cast<double>(L);
-    const uint32_t target = static_cast<uint32_t>(ceil(ks + 4.0 * sqrt(ks) + 8.0));
-    if (target > S) return false;
-    find_bin(hist, kBins, target, warp_sums, s_bin, s_above);
-    const int b0 = static_cast<int>(*s_bin);
-    if (b0 == 0) return false;  // the bound would keep every score
-    // ---- one pass: every score in bin >= b0 joins the list
-    const int64_t seg = ((L + kTopkWarps - 1) / kTopkWarps + 31) / 32 * 32;
-    const int64_t lo = min(L, seg * warp), hi = min(L, seg * (warp + 1));
-    const uint32_t lt_mask = (1u << lane) - 1u;
-    int nchunk = 0;
-    bool chunk_overflow = false;
-    for (int64_t base0 = lo; base0 < hi; base0 += 32 * kBatch) {
-        float v[kBatch];
-#pragma unroll
-        for (int e = 0; e < kBatch; ++e) {
-            const int64_t j = base0 + 32 * e + lane;
-            v[e] = j < hi ? __ldg(src + j) : -INFINITY;
-        }
-        uint32_t m[kBatch];
-        uint32_t total = 0;
-#pragma unroll
-        for (int e = 0; e < kBatch; ++e) {
-            const int64_t j = base0 + 32 * e + lane;
-            m[e] = __ballot_sync(0xFFFFFFFFu, j < hi && bin_of(v[e]) >= b0);
-            total += __popc(m[e]);
-        }
-        if (total == 0) continue;
-        uint32_t pos0 = 0;
-        if (lane == 0) pos0 = atomicAdd(s_cnt, total);
-        pos0 = __shfl_sync(0xFFFFFFFFu, pos0, 0);
-        if (nchunk < kMaxChunks) {
-            if (lane == 0) chunks[warp][nchunk] = pos0;  // chunk start; its end is stored below
-        } else {
-            chunk_overflow = true;
-        }
-        ++nchunk;
-        uint32_t pos = pos0;
-#pragma unroll
-        for (int e = 0; e < kBatch; ++e) {
-            const uint32_t p = pos + __popc(m[e] & lt_mask);
-            if (((m[e] >> lane) & 1u) && p < kCandCap) {
-                cand[p] = order_key(v[e]);
-                cand_j[p] = static_cast<int32_t>(base0 + 32 * e + lane);
-            }
-            pos += __popc(m[e]);
-        }
-        if (lane == 0 && nchunk <= kMaxChunks) chunks[warp + kTopkWarps][nchunk - 1] = pos;
-    }
-    const uint32_t nch = static_cast<uint32_t>(min(nchunk, kMaxChunks));
-    if (lane == 0) w_a[warp] = chunk_overflow ? 1u : 0u;
-    __syncthreads();
-    const uint32_t cnt = *s_cnt;
-    bool bad = cnt > kCandCap || cnt < static_cast<uint32_t>(k);
-#pragma unroll
-    for (int w = 0; w < kTopkWarps; ++w) bad = bad || w_a[w] != 0;
-    if (bad) return false;
-    // ---- exact threshold among the collected scores (they include the k largest)
-    uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
-    for (uint32_t c = threadIdx.x; c < cnt; c += kTopkThreads) {
-        kmin = min(kmin, cand[c]);
-        kmax = max(kmax, cand[c]);
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        kmin = min(kmin, __shfl_xor_sync(0xFFFFFFFFu, kmin, o));
-        kmax = max(kmax, __shfl_xor_sync(0xFFFFFFFFu, kmax, o));
-    }
-    __syncthreads();
-    if (lane == 0) {
-        w_a[warp] = kmin;
-        w_b[warp] = kmax;
-    }
-    __syncthreads();
-    kmin = w_a[0];
-    kmax = w_b[0];
-#pragma unroll
-    for (int w = 1; w < kTopkWarps; ++w) {
-        kmin = min(kmin, w_a[w]);
-        kmax = max(kmax, w_b[w]);
-    }
-    const int low_bits = kmin == kmax ? 0 : 32 - __clz(kmin ^ kmax);
-    uint32_t thr, need_eq;
-    radix_select([&](int64_t c) { return cand[c]; }, cnt, static_cast<uint32_t>(k), low_bits, kmin,
-                 hist, warp_sums, s_bin, s_above, &thr, &need_eq);
-    // ---- per warp: counts above / equal to the threshold over its own chunks
-    uint32_t ngt = 0, neq = 0;
-    for (uint32_t c = 0; c < nch; ++c) {
-        const uint32_t b = chunks[warp][c], e = chunks[warp + kTopkWarps][c];
-        for (uint32_t q = b + lane; q < e; q += 32) {
-            ngt += cand[q] > thr;
-            neq += cand[q] == thr;
-        }
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-        ngt += __shfl_xor_sync(0xFFFFFFFFu, ngt, o);
-        neq += __shfl_xor_sync(0xFFFFFFFFu, neq, o);
-    }
-    __syncthreads();
-    if (lane == 0) {
-        w_a[warp] = ngt;
-        w_b[warp] = neq;
-    }
-    __syncthreads();
-    uint32_t base_gt = 0, base_eq = 0;
-    for (int w = 0; w < warp; ++w) {
-        base_gt += w_a[w];
-        base_eq += w_b[w];
-    }
-    // ---- write this warp's kept entries in index order
-    for (uint32_t c = 0; c < nch; ++c) {
-        const uint32_t b = chunks[warp][c], e = chunks[warp + kTopkWarps][c];
-        for (uint32_t q0 = b; q0 < e; q0 += 32) {
-            const uint32_t q = q0 + lane;
-            const uint32_t u = q < e ? cand[q] : 0u;
-            const bool gt = q < e && u > thr;
-            const bool eq = q < e && u == thr;
-            const uint32_t mg = __ballot_sync(0xFFFFFFFFu, gt);
-            const uint32_t me = __ballot_sync(0xFFFFFFFFu, eq);
-            const uint32_t eq_before = base_eq + __popc(me & lt_mask);
-            if (gt || (eq && eq_before < need_eq))
-                out[base_gt + __popc(mg & lt_mask) + min(eq_before, need_eq)] = cand_j[q];
-            base_gt += __popc(mg);
-            base_eq += __popc(me);
-        }
-    }
-    return true;
-}
-
 // One CTA per query row; every pass walks the row in per-warp contiguous
 // segments (coalesced, and the last pass must emit in index order).
-__global__ void __launch_bounds__(kTopkThreads, 4)
+__global__ void __launch_bounds__(kTopkThreads)
     topk_kernel(const float *__restrict__ scores, int64_t stride, int64_t n, int64_t offset,
                 int32_t ratio, int64_t r0, int32_t k, int32_t *__restrict__ sel) {
     __shared__ uint32_t hist[kBins];
@@ -660,7 +439,6 @@ __global__ void __launch_bounds__(kTopkThreads, 4)
     __shared__ uint32_t s_bin, s_above, s_cnt;
     __shared__ float s_min[kTopkWarps], s_max[kTopkWarps];
     __shared__ uint32_t w_gt[kTopkWarps], w_eq[kTopkWarps];
-    __shared__ uint32_t chunks[2 * kTopkWarps][kMaxChunks];  // chunk starts, then chunk ends
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int row = blockIdx.x;
@@ -672,12 +450,6 @@ __global__ void __launch_bounds__(kTopkThreads, 4)
         return;
     }
     const float *src = scores + static_cast<int64_t>(row) * stride;
-    if (k <= kCandCap / 2 && L >= 4 * static_cast<int64_t>(k)) {
-        if (topk_sampled(src, L, k, out, hist, cand, cand_j, warp_sums, &s_bin, &s_above, &s_cnt,
-                         s_min, s_max, w_gt, w_eq, chunks))
-            return;
-        __syncthreads();  // the exact path below reuses the shared arrays
-    }
     const int64_t seg = ((L + kTopkWarps - 1) / kTopkWarps + 31) / 32 * 32;
     const int64_t lo = min(L, seg * warp), hi = min(L, seg * (warp + 1));
 
@@ -746,37 +518,8 @@ __global__ void __launch_bounds__(kTopkThreads, 4)
         __syncthreads();
         const uint32_t cnt = s_cnt;
         if (cnt <= kCandCap) {
-            // the candidates' common key prefix
-            uint32_t kmin = 0xFFFFFFFFu, kmax = 0u;
-            for (uint32_t c = threadIdx.x; c < cnt; c += kTopkThreads) {
-                kmin = min(kmin, cand[c]);
-                kmax = max(kmax, cand[c]);
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) {
-                kmin = min(kmin, __shfl_xor_sync(0xFFFFFFFFu, kmin, o));
-                kmax = max(kmax, __shfl_xor_sync(0xFFFFFFFFu, kmax, o));
-            }
-            if (lane == 0) {
-                w_gt[warp] = kmin;
-                w_eq[warp] = kmax;
-            }
-            __syncthreads();
-            kmin = w_gt[0];
-            kmax = w_eq[0];
-#pragma unroll
-            for (int w = 1; w < kTopkWarps; ++w) {
-                kmin = min(kmin, w_gt[w]);
-                kmax = max(kmax, w_eq[w]);
-            }
-            __syncthreads();
-            if (lane == 0) {
-                w_gt[warp] = above;
-                w_eq[warp] = 0;
-            }
-            const int low_bits = kmin == kmax ? 0 : 32 - __clz(kmin ^ kmax);
-            radix_select([&](int64_t c) { return cand[c]; }, cnt, need, low_bits, kmin, hist,
-                         warp_sums, &s_bin, &s_above, &thr, &need_eq);
+            radix_select([&](int64_t c) { return cand[c]; }, cnt, need, hist, warp_sums, &s_bin,
+                         &s_above, &thr, &need_eq);
             // candidates above / equal to the threshold, by segment
             for (uint32_t c = threadIdx.x; c < cnt; c += kTopkThreads) {
                 const int w = static_cast<int>(cand_j[c] / seg);
@@ -787,7 +530,7 @@ __global__ void __launch_bounds__(kTopkThreads, 4)
             counted = true;
         } else {
             radix_select([&](int64_t j) { return order_key(src[j]); }, L, static_cast<uint32_t>(k),
-                         32, 0u, hist, warp_sums, &s_bin, &s_above, &thr, &need_eq);
+                         hist, warp_sums, &s_bin, &s_above, &thr, &need_eq);
         }
     }
 
