@@ -75,6 +75,7 @@ constexpr uint32_t kOCol = 256;  // O^T: 4 d-tiles x 64 columns
 constexpr float kRescale = 8.0f;
 
 struct AttnParams {
+    __nv_bfloat16 *out;  // [T, 64, 512]
     const __nv_bfloat16 *raw_kv;
     const __nv_bfloat16 *pooled_kv;
     const int32_t *sel;
@@ -148,14 +149,6 @@ __device__ __forceinline__ void cp_async_arrive(uint64_t *bar) {
                  : "memory");
 }
 
-__device__ __forceinline__ void tma_store_2d(const CUtensorMap *tm, const void *src, int x, int y) {
-    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-                     tm),
-                 "r"(smem_u32(src)), "r"(x), "r"(y)
-                 : "memory");
-    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
-}
-
 // tcgen05.mma / tcgen05.commit executed by every lane of a converged warp but
 // issued only where `issue` is non-zero (one lane): the warp stays converged,
 // so the operand descriptors can stay in uniform registers.
@@ -185,8 +178,7 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
 }
 
 __global__ void __launch_bounds__(kAttnThreads, 1)
-    attn_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_out,
-                const AttnParams p) {
+    attn_kernel(const __grid_constant__ CUtensorMap tm_q, const AttnParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -406,7 +398,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int hb = 32 * hh;
         const int kl = sp * 32 + lane;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(sp * 32) << 16);
-        __nv_bfloat16 *sO = reinterpret_cast<__nv_bfloat16 *>(sP);
         int tok = 0, g = 0, cur = 0;
         for (int i = blockIdx.x; i < p.T; i += gridDim.x, ++tok) {
             const TokenInfo x = token_info(p, i);
@@ -525,8 +516,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 mbar_arrive(p_full);
             }
             // ---- token end: sums over keys, then O^T / sum -> out[t, h, d]
-            const bool live = mbar_wait(o_full, tok & 1, abort_flag, p.status);
-            tc_fence_after();
             // transpose-reduce the 32 partial sums across the warp: lane ends with
             // the warp's total for head hb + lane
 #pragma unroll
@@ -567,31 +556,31 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             bar_soft();
             if (st < 64) sLinv[st] = 1.0f / (sL[st] + sL[64 + st] + sL[128 + st] + sL[192 + st]);
             bar_soft();
-            // four [64 heads x 128 dims] tiles staged in sP, each written by one TMA store
+            // O^T (4 d-tiles x this warp's 32 heads) into registers one tile at a time, scaled
+            // and stored straight to global memory: lane holds dim d = 128m + 32sp + lane of
+            // heads hb..hb+31, so for each head the warp writes 32 consecutive dims (64
+            // contiguous bytes). No staging in shared memory, so P's buffer stays free.
+            const bool live = mbar_wait(o_full, tok & 1, abort_flag, p.status);
+            tc_fence_after();
+            __nv_bfloat16 *orow = p.out + (static_cast<int64_t>(i) * kH + hb) * kD + 32 * sp + lane;
 #pragma unroll 1
             for (int m = 0; m < 4; ++m) {
-                if (st == 0 && m > 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-                bar_soft();
+                uint32_t oa[32];
                 if (live) {
-                    uint32_t oa[32];
                     tmem_ld32(lane_base + kOCol + 64 * m + hb, oa);
                     tmem_wait_ld();
+                }
+                if (live) {
+                    __nv_bfloat16 *o = orow + 128 * m;
 #pragma unroll
                     for (int h = 0; h < 32; ++h)
-                        sO[(hb + h) * 128 + kl] =
-                            __float2bfloat16_rn(__uint_as_float(oa[h]) * sLinv[hb + h]);
+                        o[h * kD] = __float2bfloat16_rn(__uint_as_float(oa[h]) * sLinv[hb + h]);
                 }
-                fence_proxy_async_smem();
-                bar_soft();
-                if (st == 0 && live) tma_store_2d(&tm_out, sP, 128 * m, i * 64);
             }
-            // sP is reused for P^T by the next token: its last store must have read it
-            if (st == 0) asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(o_free);
         }
-        if (st == 0) asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     }
     __syncthreads();
     if (warp == kPvWarp) {
@@ -619,13 +608,11 @@ int launch_attention(const void *q, const void *raw_kv, int64_t raw_start, int64
             return DSA_ERR_CUDA;
         checked = true;
     }
-    CUtensorMap tm_q, tm_out;
+    CUtensorMap tm_q;
     if (!make_tmap_bf16(&tm_q, q, kD, static_cast<uint64_t>(chunk) * kH, kD * 2, 64, 64))
         return DSA_ERR_CUDA;
-    if (!make_tmap_bf16(&tm_out, out, kD, static_cast<uint64_t>(chunk) * kH, kD * 2, 128, 64,
-                        false))
-        return DSA_ERR_CUDA;
     AttnParams p;
+    p.out = static_cast<__nv_bfloat16 *>(out);
     p.raw_kv = static_cast<const __nv_bfloat16 *>(raw_kv);
     p.pooled_kv = static_cast<const __nv_bfloat16 *>(pooled_kv);
     p.sel = sel;
@@ -639,7 +626,7 @@ int launch_attention(const void *q, const void *raw_kv, int64_t raw_start, int64
     p.T = static_cast<int>(chunk);
     p.status = status;
     const int grid = static_cast<int>(std::min<int64_t>(chunk, std::max(1, sm_count())));
-    attn_kernel<<<grid, kAttnThreads, kAttnSmem, s>>>(tm_q, tm_out, p);
+    attn_kernel<<<grid, kAttnThreads, kAttnSmem, s>>>(tm_q, p);
     return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
