@@ -99,13 +99,13 @@ extern "C" int dsa_prefill_chunk(dsa_pool_state *st, const void *raw_kv, int64_t
 namespace {
 
 struct Events {
-    cudaEvent_t e[8] = {};
+    cudaEvent_t e[12] = {};
     int n = 0;
     ~Events() {
         for (int i = 0; i < n; ++i) cudaEventDestroy(e[i]);  // released once complete
     }
     cudaEvent_t make() {
-        if (n == 8 || cudaEventCreateWithFlags(&e[n], cudaEventDisableTiming) != cudaSuccess)
+        if (n == 12 || cudaEventCreateWithFlags(&e[n], cudaEventDisableTiming) != cudaSuccess)
             return nullptr;
         return e[n++];
     }
@@ -159,11 +159,28 @@ extern "C" int dsa_prefill_chunk_host(dsa_pool_state *st, const dsa_prefill_work
     ok = ok && cudaStreamWaitEvent(s, q_done, 0) == cudaSuccess;
     if (!ok) return DSA_ERR_CUDA;
 
-    // attention in row slices; each slice's output goes back while the next computes
-    const int slices = chunk >= 2048 ? 4 : (chunk >= 1024 ? 2 : 1);
-    const int64_t per = (chunk + slices - 1) / slices;
-    for (int64_t r0 = 0; r0 < chunk; r0 += per) {
-        const int64_t rows = chunk - r0 < per ? chunk - r0 : per;
+    // attention in row slices; each slice's output goes back while the next computes.
+    // Slices shrink towards the end (whole waves of one row per SM where possible), so
+    // the copy left exposed after the last kernel is short: the output copy of a slice
+    // takes about 0.75 of the kernel time of a slice of the same size, so each slice
+    // may be about 0.75 of the one before it.
+    int64_t cuts[8];
+    int ncut = 0;
+    {
+        const int64_t sms = sm_count() > 0 ? sm_count() : 1;
+        const int64_t waves = (chunk + sms - 1) / sms;
+        static const double kCum[] = {0.30, 0.56, 0.78, 0.92};
+        if (chunk >= 1024) {
+            for (double f : kCum) {
+                const int64_t r = static_cast<int64_t>(f * static_cast<double>(waves) + 0.5) * sms;
+                if (r > (ncut ? cuts[ncut - 1] : 0) && r < chunk) cuts[ncut++] = r;
+            }
+        }
+        cuts[ncut++] = chunk;
+    }
+    for (int ci = 0; ci < ncut; ++ci) {
+        const int64_t r0 = ci ? cuts[ci - 1] : 0;
+        const int64_t rows = cuts[ci] - r0;
         rc = launch_attention(static_cast<const uint8_t *>(ws->q) + r0 * q_row, ws->raw_kv,
                               raw_start, raw_rows, st->pooled_kv, st->n_pooled_kv,
                               ws->sel + r0 * index_topk, index_topk, rows, offset + r0,

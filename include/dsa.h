@@ -253,8 +253,9 @@ typedef struct dsa_prefill_workspace {
  *   that overlap compute (the query copy, the selection and output copies), or
  *   the same stream to serialize everything. Ordering: the inputs are copied
  *   on `stream`, the query rows on copy_stream while the pooling and indexer
- *   run, the attention runs in up to four row slices and each slice's output
- *   is copied back on copy_stream while the next slice computes. When `stream`
+ *   run, the attention runs in up to five row slices of shrinking size and
+ *   each slice's output is copied back on copy_stream while the next slice
+ *   computes. When `stream`
  *   completes, every copy has completed and the host outputs are valid.
  *   The host buffers must stay alive and unmodified until then.
  * Errors: those of dsa_prefill_chunk; DSA_ERR_ARG for a null host pointer or
