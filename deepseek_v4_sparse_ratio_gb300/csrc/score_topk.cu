@@ -405,28 +405,6 @@ __device__ __forceinline__ void radix_select(KeyAt key_at, int64_t count, uint32
     *need_out = need;
 }
 
-// Eight loads of a warp-strided walk issued together (more bytes in flight per
-// thread: the passes are bound by load latency, not bandwidth).
-constexpr int kBatch = 8;
-
-template <typename F>
-__device__ __forceinline__ void walk(const float *__restrict__ src, int64_t lo, int64_t hi, F f) {
-    const int lane = threadIdx.x & 31;
-    for (int64_t base = lo + lane; base < hi; base += 32 * kBatch) {
-        float v[kBatch];
-#pragma unroll
-        for (int e = 0; e < kBatch; ++e) {
-            const int64_t j = base + 32 * e;
-            v[e] = j < hi ? __ldg(src + j) : 0.0f;
-        }
-#pragma unroll
-        for (int e = 0; e < kBatch; ++e) {
-            const int64_t j = base + 32 * e;
-            if (j < hi) f(v[e], j);
-        }
-    }
-}
-
 // One CTA per query row; every pass walks the row in per-warp contiguous
 // segments (coalesced, and the last pass must emit in index order).
 __global__ void __launch_bounds__(kTopkThreads)
@@ -455,10 +433,11 @@ __global__ void __launch_bounds__(kTopkThreads)
 
     // ---- 1. range of the row
     float vmin = INFINITY, vmax = -INFINITY;
-    walk(src, lo, hi, [&](float v, int64_t) {
+    for (int64_t j = lo + lane; j < hi; j += 32) {
+        const float v = src[j];
         vmin = fminf(vmin, v);
         vmax = fmaxf(vmax, v);
-    });
+    }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
         vmin = fminf(vmin, __shfl_xor_sync(0xFFFFFFFFu, vmin, o));
@@ -490,7 +469,7 @@ __global__ void __launch_bounds__(kTopkThreads)
         // of a higher bin is >= every element of a lower bin
         const float scale = static_cast<float>(kBins) / (vmax - vmin);
         auto bin_of = [&](float v) { return min(kBins - 1, static_cast<int>((v - vmin) * scale)); };
-        walk(src, lo, hi, [&](float v, int64_t) { atomicAdd(&hist[bin_of(v)], 1u); });
+        for (int64_t j = lo + lane; j < hi; j += 32) atomicAdd(&hist[bin_of(src[j])], 1u);
         __syncthreads();
         find_bin(hist, kBins, static_cast<uint32_t>(k), warp_sums, &s_bin, &s_above);
         const int bstar = static_cast<int>(s_bin);
@@ -498,7 +477,8 @@ __global__ void __launch_bounds__(kTopkThreads)
         // ---- 3. the threshold bin's elements are the candidates; count each
         // segment's elements above that bin on the way
         uint32_t above = 0;
-        walk(src, lo, hi, [&](float v, int64_t j) {
+        for (int64_t j = lo + lane; j < hi; j += 32) {
+            const float v = src[j];
             const int b = bin_of(v);
             above += b > bstar;
             if (b == bstar) {
@@ -508,7 +488,7 @@ __global__ void __launch_bounds__(kTopkThreads)
                     cand_j[c] = static_cast<int32_t>(j);
                 }
             }
-        });
+        }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) above += __shfl_xor_sync(0xFFFFFFFFu, above, o);
         if (lane == 0) {
@@ -555,27 +535,18 @@ __global__ void __launch_bounds__(kTopkThreads)
         base_eq += w_eq[w];
     }
     const uint32_t lt_mask = (1u << lane) - 1u;
-    for (int64_t base0 = lo; base0 < hi; base0 += 32 * kBatch) {
-        uint32_t uv[kBatch];
-#pragma unroll
-        for (int e = 0; e < kBatch; ++e) {
-            const int64_t j = base0 + 32 * e + lane;
-            uv[e] = j < hi ? order_key(__ldg(src + j)) : 0u;
-        }
-#pragma unroll
-        for (int e = 0; e < kBatch; ++e) {
-            const int64_t j = base0 + 32 * e + lane;
-            const bool gt = j < hi && uv[e] > thr;
-            const bool eq = j < hi && uv[e] == thr;
-            const uint32_t mg = __ballot_sync(0xFFFFFFFFu, gt);
-            const uint32_t me = __ballot_sync(0xFFFFFFFFu, eq);
-            const uint32_t eq_before = base_eq + __popc(me & lt_mask);
-            if (gt || (eq && eq_before < need_eq))
-                out[base_gt + __popc(mg & lt_mask) + min(eq_before, need_eq)] =
-                    static_cast<int32_t>(j);
-            base_gt += __popc(mg);
-            base_eq += __popc(me);
-        }
+    for (int64_t base = lo; base < hi; base += 32) {
+        const int64_t j = base + lane;
+        const uint32_t u = j < hi ? order_key(src[j]) : 0u;
+        const bool gt = j < hi && u > thr;
+        const bool eq = j < hi && u == thr;
+        const uint32_t mg = __ballot_sync(0xFFFFFFFFu, gt);
+        const uint32_t me = __ballot_sync(0xFFFFFFFFu, eq);
+        const uint32_t eq_before = base_eq + __popc(me & lt_mask);
+        if (gt || (eq && eq_before < need_eq))
+            out[base_gt + __popc(mg & lt_mask) + min(eq_before, need_eq)] = static_cast<int32_t>(j);
+        base_gt += __popc(mg);
+        base_eq += __popc(me);
     }
 }
 
