@@ -62,14 +62,20 @@ constexpr int kRegsSoft = 176;
 constexpr int kSoftThreads = 256;
 constexpr uint32_t kOffQ = 0;                 // 8 chunks x [64 heads x 128 B]
 constexpr uint32_t kOffKV = 65536;            // 8 chunks x [128 keys x 128 B]
-constexpr uint32_t kOffP = 65536 + 131072;    // P^T [128 keys x 64 heads] bf16; output staging
-constexpr uint32_t kOffRed = kOffP + 16384;   // [4 sub-partitions][64] fp32 block maxima
-constexpr uint32_t kOffL = kOffRed + 1024;    // [4][64] fp32 partial sums
-constexpr uint32_t kOffLinv = kOffL + 1024;   // [64] 1/sum
+constexpr uint32_t kOffP = 65536 + 131072;    // P^T [128 keys x 64 heads] bf16
+// A ninth key chunk slot: chunk 7 (dims 448..511) of odd blocks lives here, of even
+// blocks in its usual slot, so a block's chunk 7 can land while the block before it
+// still holds all eight usual slots; after the previous PV only chunk 6 is left to load.
+constexpr uint32_t kOffX = kOffP + 16384;
+// The per-block scratch of the rescale path and the per-token one of the epilogue are
+// never live together (nor for the same heads), so they share space.
+constexpr uint32_t kOffRed = kOffX + 16384;   // [4][64] block maxima  |  partial sums
+constexpr uint32_t kOffLinv = kOffRed + 1024; // [64] rescale factors  |  1/sum
 constexpr uint32_t kOffM = kOffLinv + 256;    // [2][64] running max (double-buffered)
-constexpr uint32_t kOffAlpha = kOffM + 512;   // [64] rescale factors
-constexpr uint32_t kOffBar = kOffAlpha + 256;
-constexpr uint32_t kAttnSmem = kOffBar + 256 + 1024;
+constexpr uint32_t kOffBar = kOffM + 512;
+constexpr uint32_t kAttnSmem = kOffBar + 256 + 1024;  // + slack for 1024-B alignment
+static_assert(kAttnSmem <= 232448, "over the shared memory of one CTA");
+constexpr uint32_t kLbo7Spare = kOffX - (kOffKV + 6 * 16384);  // chunk 6 -> spare chunk 7
 constexpr uint32_t kSCol = 0;    // S^T: 64 TMEM columns
 constexpr uint32_t kOCol = 256;  // O^T: 4 d-tiles x 64 columns
 constexpr float kRescale = 8.0f;
@@ -186,15 +192,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     uint8_t *sKV = smem + kOffKV;
     uint8_t *sP = smem + kOffP;
     float *sRed = reinterpret_cast<float *>(smem + kOffRed);
-    float *sL = reinterpret_cast<float *>(smem + kOffL);
+    float *sL = reinterpret_cast<float *>(smem + kOffRed);
     float *sLinv = reinterpret_cast<float *>(smem + kOffLinv);
     float *sM = reinterpret_cast<float *>(smem + kOffM);
-    float *sAlpha = reinterpret_cast<float *>(smem + kOffAlpha);
+    float *sAlpha = reinterpret_cast<float *>(smem + kOffLinv);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
     uint64_t *q_full = bars + 0;
     uint64_t *q_free = bars + 1;
-    uint64_t *kv_full = bars + 2;   // [4] chunk pair landed
-    uint64_t *kv_free = bars + 10;  // [4] chunk pair (d-tile) consumed by PV
+    uint64_t *kv_full = bars + 2;   // [4] chunk pairs 0-2, then chunk 6, landed
+    uint64_t *x_full = bars + 6;    // [2] chunk 7 landed, by block parity (usual / spare slot)
+    uint64_t *x_free = bars + 8;    // [2] chunk 7 slot consumed by PV
+    uint64_t *kv_free = bars + 10;  // [4] chunk pairs 0-2, then chunk 6, consumed by PV
     uint64_t *s_full = bars + 14;
     uint64_t *p_full = bars + 15;
     uint64_t *o_full = bars + 16;
@@ -210,6 +218,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         mbar_init(q_free, 1);
         for (int m = 0; m < 4; ++m) mbar_init(&kv_full[m], 32 * kLoadWarps);  // noinc arrivals
         for (int m = 0; m < 4; ++m) mbar_init(&kv_free[m], 1);
+        for (int q = 0; q < 2; ++q) {
+            mbar_init(&x_full[q], 32 * kLoadWarps);
+            mbar_init(&x_free[q], 1);
+        }
         // a block's S^T is ready once its QK is done (QK warp) and the previous
         // block's PV no longer reads P or writes O^T (PV warp)
         mbar_init(s_full, 2);
@@ -239,6 +251,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int lw = warp;
         const uint64_t pol_stream = policy_evict_first();
         const uint32_t kv_base = smem_u32(sKV);
+        const uint32_t x_base = smem_u32(smem + kOffX);
         const int a = lane >> 3, pc = lane & 7;
         const int ngroups = (32 - lw + kLoadWarps - 1) / kLoadWarps;
         const bool holder = lane < 4 * ngroups;
@@ -281,6 +294,25 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 const int row = row_of(x, b, jn);
                 const uint8_t *src_base =
                     reinterpret_cast<const uint8_t *>(b < x.nwb ? p.raw_kv : p.pooled_kv) + pc * 16;
+                const int par = g & 1;
+                // chunk 7 first: its slot (usual one for even blocks, spare for odd ones)
+                // was released by the PV two blocks back
+                if (lane == 0)
+                    ok = mbar_wait(&x_free[par], ((g >> 1) & 1) ^ 1, abort_flag, p.status);
+                ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+                if (!ok) break;
+#pragma unroll 1
+                for (int gq = 0; gq < ngroups; ++gq) {
+                    const int r = 4 * (lw + kLoadWarps * gq) + a;
+                    const int srow = __shfl_sync(0xFFFFFFFFu, row, 4 * gq + a);
+                    const uint8_t *src = src_base + static_cast<int64_t>(srow) * (kD * 2);
+                    const uint32_t off = r * 128 + ((pc ^ (r & 7)) << 4);
+                    cp_async16((par ? x_base : kv_base + 7 * 16384) + off, src + 7 * 128);
+                }
+                cp_async_arrive(&x_full[par]);
+                jn = (b + 1 < x.nb) ? fetch(x, i, b + 1)
+                                    : (inext < p.T ? fetch(xnext, inext, 0) : -1);
+                // chunk pairs 0-2, then chunk 6, as the previous block's PV releases them
                 for (int m = 0; m < 4 && ok; ++m) {
                     if (lane == 0) ok = mbar_wait(&kv_free[m], (g & 1) ^ 1, abort_flag, p.status);
                     ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
@@ -292,12 +324,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         const uint8_t *src = src_base + static_cast<int64_t>(srow) * (kD * 2);
                         const uint32_t dst = kv_base + r * 128 + ((pc ^ (r & 7)) << 4);
                         cp_async16(dst + (2 * m) * 16384, src + (2 * m) * 128);
-                        cp_async16(dst + (2 * m + 1) * 16384, src + (2 * m + 1) * 128);
+                        if (m < 3) cp_async16(dst + (2 * m + 1) * 16384, src + (2 * m + 1) * 128);
                     }
                     cp_async_arrive(&kv_full[m]);
-                    if (m == 0)
-                        jn = (b + 1 < x.nb) ? fetch(x, i, b + 1)
-                                            : (inext < p.T ? fetch(xnext, inext, 0) : -1);
                 }
             }
             x = xnext;
@@ -312,6 +341,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const uint32_t leader = lane == 0;
         constexpr uint32_t idesc_qk = idesc_bf16(128, 64, false, false);
         const uint64_t ad0 = desc_sw128(smem_u32(sKV), 16, 1024);
+        const uint64_t adx = desc_sw128(smem_u32(smem + kOffX), 16, 1024);
         const uint64_t bd0 = desc_sw128(smem_u32(sQ), 16, 1024);
         int tok = 0, g = 0;
         bool ok = true;
@@ -322,11 +352,25 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             for (int b = 0; b < x.nb && ok; ++b, ++g) {
                 // S^T is single-buffered: the softmax of the previous block must have read it
                 if (g > 0 && !(ok = mbar_wait(p_full, (g - 1) & 1, abort_flag, p.status))) break;
+                // chunk 7 landed early (usual slot on even blocks, spare slot on odd ones)
+                const int par = g & 1;
+                if (!(ok = mbar_wait(&x_full[par], (g >> 1) & 1, abort_flag, p.status))) break;
+                // rows landed through the generic proxy; the MMA reads via the async proxy
+                fence_proxy_async_smem();
+                tc_fence_after();
+                {
+                    const uint64_t ad = par ? adx : ad0 + ((7 * 16384) >> 4);
+                    const uint64_t bd = bd0 + ((7 * 8192) >> 4);
+#pragma unroll
+                    for (int kk = 0; kk < 4; ++kk)
+                        mma_bf16_if(tmem + kSCol, ad + 2 * kk, bd + 2 * kk, idesc_qk, kk != 0,
+                                    leader);
+                }
 #pragma unroll 1
                 for (int m = 0; m < 4; ++m) {
-                    // one wait per chunk pair: a wait stalls this warp's MMA issue
+                    // one wait per chunk pair (chunk 6 alone last): a wait stalls this warp's
+                    // MMA issue
                     if (!(ok = mbar_wait(&kv_full[m], g & 1, abort_flag, p.status))) break;
-                    // rows landed through the generic proxy; the MMA reads via the async proxy
                     fence_proxy_async_smem();
                     tc_fence_after();
                     const uint64_t ad = ad0 + ((2 * m * 16384) >> 4);
@@ -335,9 +379,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     for (int h = 0; h < 2; ++h)
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
-                            mma_bf16_if(tmem + kSCol, ad + ((h * 16384) >> 4) + 2 * kk,
-                                        bd + ((h * 8192) >> 4) + 2 * kk, idesc_qk,
-                                        (m | h | kk) != 0, leader);
+                            if (m < 3 || h == 0)
+                                mma_bf16_if(tmem + kSCol, ad + ((h * 16384) >> 4) + 2 * kk,
+                                            bd + ((h * 8192) >> 4) + 2 * kk, idesc_qk, 1u,
+                                            leader);
                 }
                 if (!ok) break;
                 mma_commit_if(s_full, leader);
@@ -367,16 +412,20 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     tc_fence_after();
                 }
                 const uint32_t acc0 = b > 0;
+                // d-tile 3 is chunks 6 and 7: on odd blocks chunk 7 sits in the spare slot
+                const uint32_t lbo3 = (g & 1) ? kLbo7Spare : 16384u;
                 if (leader) {
 #pragma unroll
                     for (int m = 0; m < 4; ++m) {
 #pragma unroll
                         for (int kk = 0; kk < 8; ++kk)
                             mma_bf16(tmem + kOCol + 64 * m,
-                                     desc_sw128(smem_u32(sKV + 2 * m * 16384 + kk * 2048), 16384, 1024),
+                                     desc_sw128(smem_u32(sKV + 2 * m * 16384 + kk * 2048),
+                                                m < 3 ? 16384u : lbo3, 1024),
                                      desc_sw128(smem_u32(sP + kk * 2048), 8192, 1024), idesc_pv,
                                      kk > 0 ? 1u : acc0);
                         mma_commit(&kv_free[m]);
+                        if (m == 3) mma_commit(&x_free[g & 1]);
                     }
                 }
                 __syncwarp();
