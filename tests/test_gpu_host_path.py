@@ -14,10 +14,22 @@ from deepseek_v4_sparse_ratio_gb300.runner import DeviceWorkload
 pytestmark = pytest.mark.gpu
 
 
+def _small(kind):
+    if kind == "skip_then_full":      # 130 rows fit k (skip path), then 70 more do not
+        return inputs.small(31, [130, 70], index_topk=40)
+    if kind == "decode":              # a prefill, then single-row chunks
+        return inputs.small(32, [300, 1, 1, 1], index_topk=16)
+    return inputs.workload(kind)
+
+
 @pytest.mark.parametrize("name,copy_stream", [("two_chunks_4098", True),
-                                              ("two_chunks_4098", False)])
+                                              ("two_chunks_4098", False),
+                                              ("skip_then_full", True),
+                                              ("decode", True)])
 def test_host_path_equals_device_path(dsa, name, copy_stream):
-    wl = inputs.draw(inputs.workload(name))
+    wl = inputs.draw(_small(name))
+    if not wl.tile_rows:
+        wl.tile_rows = (64,)
     dw = DeviceWorkload(wl, tile_rows=wl.tile_rows[0])
     W = wl.window
     raw_all = torch.cat([wl.t["prefix_win"], wl.t["raw_kv"]], 0).pin_memory()
