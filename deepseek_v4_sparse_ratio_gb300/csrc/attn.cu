@@ -201,7 +201,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     uint64_t *q_free = bars + 1;
     uint64_t *kv_full = bars + 2;   // [4] chunk pairs 0-2, then chunk 6, landed
     uint64_t *x_full = bars + 6;    // [2] chunk 7 landed, by block parity (usual / spare slot)
-    uint64_t *x_free = bars + 8;    // [2] chunk 7 slot consumed by PV
     uint64_t *kv_free = bars + 10;  // [4] chunk pairs 0-2, then chunk 6, consumed by PV
     uint64_t *s_full = bars + 14;
     uint64_t *p_full = bars + 15;
@@ -218,10 +217,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         mbar_init(q_free, 1);
         for (int m = 0; m < 4; ++m) mbar_init(&kv_full[m], 32 * kLoadWarps);  // noinc arrivals
         for (int m = 0; m < 4; ++m) mbar_init(&kv_free[m], 1);
-        for (int q = 0; q < 2; ++q) {
-            mbar_init(&x_full[q], 32 * kLoadWarps);
-            mbar_init(&x_free[q], 1);
-        }
+        for (int q = 0; q < 2; ++q) mbar_init(&x_full[q], 32 * kLoadWarps);
         // a block's S^T is ready once its QK is done (QK warp) and the previous
         // block's PV no longer reads P or writes O^T (PV warp)
         mbar_init(s_full, 2);
@@ -295,12 +291,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 const uint8_t *src_base =
                     reinterpret_cast<const uint8_t *>(b < x.nwb ? p.raw_kv : p.pooled_kv) + pc * 16;
                 const int par = g & 1;
-                // chunk 7 first: its slot (usual one for even blocks, spare for odd ones)
-                // was released by the PV two blocks back
-                if (lane == 0)
-                    ok = mbar_wait(&x_free[par], ((g >> 1) & 1) ^ 1, abort_flag, p.status);
-                ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-                if (!ok) break;
+                // chunk 7 first, into the slot (usual one for even blocks, spare for odd
+                // ones) of the block two back: this warp already waited for that block's
+                // last PV tile before loading the previous block's chunk 6
+
 #pragma unroll 1
                 for (int gq = 0; gq < ngroups; ++gq) {
                     const int r = 4 * (lw + kLoadWarps * gq) + a;
@@ -425,7 +419,6 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                                      desc_sw128(smem_u32(sP + kk * 2048), 8192, 1024), idesc_pv,
                                      kk > 0 ? 1u : acc0);
                         mma_commit(&kv_free[m]);
-                        if (m == 3) mma_commit(&x_free[g & 1]);
                     }
                 }
                 __syncwarp();
