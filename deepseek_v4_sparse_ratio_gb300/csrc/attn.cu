@@ -22,7 +22,8 @@
 // K_blk and V_blk are the same shared-memory tile (K = V): 8 chunks of
 // [128 rows x 64 dims] with 128-byte swizzle, read K-major by the first MMA and
 // MN-major by the second, filled and released in chunk pairs (one d-tile of
-// the second MMA each) so the next block's rows stream in while PV drains.
+// the second MMA each) so the next block's rows stream in while PV drains; a
+// ninth chunk slot takes chunk 7 of odd blocks so that chunk loads ahead.
 // S^T (64 columns) and O^T (4 x 64 columns) live in TMEM. Roles: six loader
 // warps, one warp issuing QK, one issuing PV, eight softmax warps that own
 // TMEM lanes = keys: they mask, run the online softmax in the log2 domain
@@ -30,7 +31,8 @@
 // max is only raised when some logit exceeds it by more than 8 (log2 units): P
 // then stays <= 256, and the rescale of O^T and of the partial sums is skipped
 // on most blocks without changing the result (the same max divides out at the
-// end). Output = O^T / sum, bf16.
+// end). Output = O^T / sum, bf16, stored by the softmax warps straight from the
+// registers they read O^T into.
 #include <math.h>
 
 #include <algorithm>
