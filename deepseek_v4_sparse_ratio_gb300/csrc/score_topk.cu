@@ -497,9 +497,32 @@ __global__ void __launch_bounds__(kTopkThreads)
         }
         __syncthreads();
         const uint32_t cnt = s_cnt;
-        if (cnt <= kCandCap) {
+        if (cnt <= kTopkThreads) {
+            // few candidates (the usual case: one linear bin near the threshold holds a
+            // handful of scores): each thread ranks one candidate against all of them;
+            // the need-th largest has fewer than `need` strictly larger keys and at
+            // least `need` larger-or-equal ones
+            if (threadIdx.x < cnt) {
+                const uint32_t u = cand[threadIdx.x];
+                uint32_t gt = 0, ge = 0;
+                for (uint32_t c = 0; c < cnt; ++c) {
+                    const uint32_t v = cand[c];
+                    gt += v > u;
+                    ge += v >= u;
+                }
+                if (gt < need && need <= ge) {  // every thread holding that key agrees
+                    s_bin = u;
+                    s_above = need - gt;
+                }
+            }
+            __syncthreads();
+            thr = s_bin;
+            need_eq = s_above;
+        } else if (cnt <= kCandCap) {
             radix_select([&](int64_t c) { return cand[c]; }, cnt, need, hist, warp_sums, &s_bin,
                          &s_above, &thr, &need_eq);
+        }
+        if (cnt <= kCandCap) {
             // candidates above / equal to the threshold, by segment
             for (uint32_t c = threadIdx.x; c < cnt; c += kTopkThreads) {
                 const int w = static_cast<int>(cand_j[c] / seg);
