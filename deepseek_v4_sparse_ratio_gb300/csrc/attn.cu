@@ -78,7 +78,7 @@ constexpr uint32_t kOffBar = kOffM + 512;
 constexpr uint32_t kAttnSmem = kOffBar + 256 + 1024;  // + slack for 1024-B alignment
 static_assert(kAttnSmem <= 232448, "over the shared memory of one CTA");
 constexpr uint32_t kLbo7Spare = kOffX - (kOffKV + 6 * 16384);  // chunk 6 -> spare chunk 7
-constexpr uint32_t kSCol = 0;    // S^T: 64 TMEM columns
+constexpr uint32_t kSCol = 0;    // S^T: 2 x 64 TMEM columns (double-buffered by block parity)
 constexpr uint32_t kOCol = 256;  // O^T: 4 d-tiles x 64 columns
 constexpr float kRescale = 8.0f;
 
@@ -203,6 +203,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     uint64_t *q_free = bars + 1;
     uint64_t *kv_full = bars + 2;   // [4] chunk pairs 0-2, then chunk 6, landed
     uint64_t *x_full = bars + 6;    // [2] chunk 7 landed, by block parity (usual / spare slot)
+    uint64_t *s_free = bars + 8;    // [2] S^T buffer read by the softmax, by block parity
     uint64_t *kv_free = bars + 10;  // [4] chunk pairs 0-2, then chunk 6, consumed by PV
     uint64_t *s_full = bars + 14;
     uint64_t *p_full = bars + 15;
@@ -219,7 +220,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         mbar_init(q_free, 1);
         for (int m = 0; m < 4; ++m) mbar_init(&kv_full[m], 32 * kLoadWarps);  // noinc arrivals
         for (int m = 0; m < 4; ++m) mbar_init(&kv_free[m], 1);
-        for (int q = 0; q < 2; ++q) mbar_init(&x_full[q], 32 * kLoadWarps);
+        for (int q = 0; q < 2; ++q) {
+            mbar_init(&x_full[q], 32 * kLoadWarps);
+            mbar_init(&s_free[q], 8);  // one arrival per softmax warp
+        }
         // a block's S^T is ready once its QK is done (QK warp) and the previous
         // block's PV no longer reads P or writes O^T (PV warp)
         mbar_init(s_full, 2);
@@ -346,10 +350,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             if (!(ok = mbar_wait(q_full, tok & 1, abort_flag, p.status))) break;
             tc_fence_after();
             for (int b = 0; b < x.nb && ok; ++b, ++g) {
-                // S^T is single-buffered: the softmax of the previous block must have read it
-                if (g > 0 && !(ok = mbar_wait(p_full, (g - 1) & 1, abort_flag, p.status))) break;
-                // chunk 7 landed early (usual slot on even blocks, spare slot on odd ones)
+                // S^T is double-buffered: the softmax of the block two back must have read
+                // this buffer; then QK can start while the previous block's softmax runs
                 const int par = g & 1;
+                if (!(ok = mbar_wait(&s_free[par], ((g >> 1) & 1) ^ 1, abort_flag, p.status)))
+                    break;
+                const uint32_t s_col = tmem + kSCol + 64 * par;
+                // chunk 7 landed early (usual slot on even blocks, spare slot on odd ones)
                 if (!(ok = mbar_wait(&x_full[par], (g >> 1) & 1, abort_flag, p.status))) break;
                 // rows landed through the generic proxy; the MMA reads via the async proxy
                 fence_proxy_async_smem();
@@ -359,7 +366,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     const uint64_t bd = bd0 + ((7 * 8192) >> 4);
 #pragma unroll
                     for (int kk = 0; kk < 4; ++kk)
-                        mma_bf16_if(tmem + kSCol, ad + 2 * kk, bd + 2 * kk, idesc_qk, kk != 0,
+                        mma_bf16_if(s_col, ad + 2 * kk, bd + 2 * kk, idesc_qk, kk != 0,
                                     leader);
                 }
 #pragma unroll 1
@@ -376,7 +383,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
                         for (int kk = 0; kk < 4; ++kk)
                             if (m < 3 || h == 0)
-                                mma_bf16_if(tmem + kSCol, ad + ((h * 16384) >> 4) + 2 * kk,
+                                mma_bf16_if(s_col, ad + ((h * 16384) >> 4) + 2 * kk,
                                             bd + ((h * 8192) >> 4) + 2 * kk, idesc_qk, 1u,
                                             leader);
                 }
@@ -466,9 +473,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 tc_fence_after();
                 uint32_t sa[32];
                 if (live) {
-                    tmem_ld32(lane_base + kSCol + hb, sa);
+                    tmem_ld32(lane_base + kSCol + 64 * (g & 1) + hb, sa);
                     tmem_wait_ld();
                 }
+                // this S^T buffer may take the QK of the block after next
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&s_free[g & 1]);
                 valid = valid && live;
                 // x = scale*log2e*logit - running max, once per (key, head); the same
                 // values decide the rescale and feed exp2
