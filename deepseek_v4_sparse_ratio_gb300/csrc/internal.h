@@ -46,12 +46,17 @@ int launch_pool_append(const dsa_pool_state &st, const void *raw_kv, const void 
                        int64_t chunk, int64_t offset, cudaStream_t s);
 int launch_fill_selection(int32_t *sel, int64_t rows, int32_t k, int64_t offset, int64_t n,
                           int32_t ratio, cudaStream_t s);
+// launch_score_tile also writes each row's per-segment score range into the
+// row's selection entries when k >= 2 x segments (sel may be null) and reports
+// the segment count in *nseg_rng (0 when it did not); launch_topk_tile then
+// takes the range from there (nseg_rng > 0) instead of a pass over the scores.
 int launch_score_tile(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const float *w,
                       int64_t n, int64_t offset, int32_t ratio, int64_t r0, int64_t R,
-                      float *scores, int64_t stride, int32_t *status, cudaStream_t s);
+                      float *scores, int64_t stride, int32_t *sel, int32_t k, int *nseg_rng,
+                      int32_t *status, cudaStream_t s);
 int launch_topk_tile(const float *scores, int64_t stride, int64_t n, int64_t offset,
-                     int32_t ratio, int64_t r0, int64_t R, int32_t k, int32_t *sel,
-                     int32_t *status, cudaStream_t s);
+                     int32_t ratio, int64_t r0, int64_t R, int32_t k, int32_t nseg_rng,
+                     int32_t *sel, int32_t *status, cudaStream_t s);
 int launch_attention(const void *q, const void *raw_kv, int64_t raw_start, int64_t raw_rows,
                      const void *pooled_kv, int64_t n, const int32_t *sel, int32_t k,
                      int64_t chunk, int64_t offset, int32_t ratio, int32_t window, float scale,

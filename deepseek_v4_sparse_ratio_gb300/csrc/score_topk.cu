@@ -22,9 +22,14 @@
 // pooled row j and reduces them in registers: ReLU, multiply by w, sum over
 // heads in order h = 0..63, mask j >= n_vis(t) to -inf, store coalesced.
 //
+// The epilogue also reduces each row's visible scores to a (min, max) per key
+// segment, parked in the row's selection entries until the top-k overwrites them.
+//
 // Top-k kernel: one CTA per query row. Rows with n_vis <= k keep all visible
-// rows. Otherwise a 3-digit (11/11/10-bit) radix select over order-preserving
-// keys of the fp32 scores finds the k-th largest value and how many of its
+// rows. Otherwise 2048 linear bins between the row's min and max (a monotone
+// map) locate the bin holding the k-th largest score; that bin's scores are the
+// candidates, among which a rank count (or, for a crowded bin, a radix select
+// over order-preserving keys) finds the k-th largest value and how many of its
 // equals to keep; a final pass in index order emits the kept indices
 // ascending, taking equal scores lowest index first.
 #include <math.h>
@@ -49,7 +54,8 @@ constexpr uint32_t kAStage = 2 * 128 * 128;      // [k-chunk][128 rows][128 B]
 constexpr uint32_t kOffB = 0;
 constexpr uint32_t kOffA = kOffB + kBBytes;
 constexpr uint32_t kOffW = kOffA + kStages * kAStage;
-constexpr uint32_t kOffBar = kOffW + kTok * kHI * 4;
+constexpr uint32_t kOffRng = kOffW + kTok * kHI * 4;  // [16 epilogue warps][4] partial ranges
+constexpr uint32_t kOffBar = kOffRng + kEpiWarps * 4 * 4;
 constexpr uint32_t kScoreSmem = kOffBar + 256 + 1024;  // + slack for 1024-B alignment
 
 struct ScoreParams {
@@ -64,6 +70,8 @@ struct ScoreParams {
     int nseg;         // key-range segments per 8-row group
     int NB;           // stride / 128
     int n_units;      // ceil(R/8) * nseg
+    int32_t *rng;     // selection rows [chunk, k] used as range scratch, or null
+    int32_t k;        // selection row length
     int32_t *status;
 };
 
@@ -93,13 +101,16 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
         if (clock64() - t0 > kWaitBudget) break;
 }
 
-__device__ __forceinline__ void store_score(const ScoreParams &p, int row, int64_t j, float acc) {
-    if (row >= p.R) return;
+// Stores the masked score of (row, pooled row j) and returns it (-inf when masked
+// or when the row is past the tile).
+__device__ __forceinline__ float store_score(const ScoreParams &p, int row, int64_t j, float acc) {
+    if (row >= p.R) return -INFINITY;
     const int64_t t = p.offset + p.r0 + row;
     const int64_t nv = min(p.n, (t + 1) / p.ratio);
     // sum of (+0) and (-0) terms can be -0; keep one zero so key order is total
     const float s = j < nv ? (acc == 0.0f ? 0.0f : acc) : -INFINITY;
     __stcs(p.scores + static_cast<int64_t>(row) * p.stride + j, s);
+    return s;
 }
 
 __global__ void __launch_bounds__(kScoreThreads, 1)
@@ -111,6 +122,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
     uint8_t *sB = smem + kOffB;
     uint8_t *sA = smem + kOffA;
     float *sW = reinterpret_cast<float *>(smem + kOffW);
+    float *sRng = reinterpret_cast<float *>(smem + kOffRng);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kOffBar);
     uint64_t *full = bars;                 // [kStages] key block landed
     uint64_t *empty = bars + kStages;      // [kStages] key block consumed by the MMAs
@@ -248,6 +260,8 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             }
             asm volatile("bar.sync 1, %0;" ::"r"(nthr) : "memory");
             bool ok = !*abort_flag;
+            // range of the visible scores of this warp's two rows (half 0 / 1)
+            float rmin0 = INFINITY, rmax0 = -INFINITY, rmin1 = INFINITY, rmax1 = -INFINITY;
             for (int kb = x.b0; kb < x.b1 && ok; ++kb) {
                 const int64_t j = static_cast<int64_t>(kb) * kScoreBlock + sp * 32 + lane;
                 if (kb < x.kend) {
@@ -295,11 +309,53 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                         }
                         float ae, ao;
                         asm("mov.b64 {%0, %1}, %2;" : "=f"(ae), "=f"(ao) : "l"(acc));
-                        store_score(p, x.row0 + ti, j, ae + ao);
+                        const float sc = store_score(p, x.row0 + ti, j, ae + ao);
+                        const float sv = sc == -INFINITY ? INFINITY : sc;
+                        if (half) {
+                            rmin1 = fminf(rmin1, sv);
+                            rmax1 = fmaxf(rmax1, sc);
+                        } else {
+                            rmin0 = fminf(rmin0, sv);
+                            rmax0 = fmaxf(rmax0, sc);
+                        }
                     }
                 } else {
                     for (int half = 0; half < 2; ++half)
                         store_score(p, x.row0 + half * 4 + tl, j, -INFINITY);
+                }
+            }
+            if (p.rng) {
+                // Each row's (min, max) over this unit's key segment goes to the row's
+                // selection entries 2s, 2s+1 (s = segment), so the top-k kernel needs no
+                // pass of its own for the range; it overwrites them with the selection.
+#pragma unroll
+                for (int o = 16; o > 0; o >>= 1) {
+                    rmin0 = fminf(rmin0, __shfl_xor_sync(0xFFFFFFFFu, rmin0, o));
+                    rmax0 = fmaxf(rmax0, __shfl_xor_sync(0xFFFFFFFFu, rmax0, o));
+                    rmin1 = fminf(rmin1, __shfl_xor_sync(0xFFFFFFFFu, rmin1, o));
+                    rmax1 = fmaxf(rmax1, __shfl_xor_sync(0xFFFFFFFFu, rmax1, o));
+                }
+                if (lane == 0) {
+                    sRng[ew * 4 + 0] = rmin0;
+                    sRng[ew * 4 + 1] = rmax0;
+                    sRng[ew * 4 + 2] = rmin1;
+                    sRng[ew * 4 + 3] = rmax1;
+                }
+                asm volatile("bar.sync 1, %0;" ::"r"(nthr) : "memory");
+                // row ti = 4 * half + tl is held by warps 4tl .. 4tl+3 (one per TMEM lane quarter)
+                const int ti = ew * 32 + lane;
+                if (ti < kTok && x.row0 + ti < p.R) {
+                    const int h = ti >> 2, tq = ti & 3;
+                    float mn = INFINITY, mx = -INFINITY;
+#pragma unroll
+                    for (int e = 4 * tq; e < 4 * tq + 4; ++e) {
+                        mn = fminf(mn, sRng[e * 4 + 2 * h]);
+                        mx = fmaxf(mx, sRng[e * 4 + 2 * h + 1]);
+                    }
+                    int32_t *dst = p.rng + (p.r0 + x.row0 + ti) * static_cast<int64_t>(p.k) +
+                                   2 * (u % p.nseg);
+                    dst[0] = __float_as_int(mn);
+                    dst[1] = __float_as_int(mx);
                 }
             }
         }
@@ -406,10 +462,13 @@ __device__ __forceinline__ void radix_select(KeyAt key_at, int64_t count, uint32
 }
 
 // One CTA per query row; every pass walks the row in per-warp contiguous
-// segments (coalesced, and the last pass must emit in index order).
+// segments (coalesced, and the last pass must emit in index order). Rows are
+// taken last first: the score kernel writes the last rows last, so theirs are
+// the scores still in L2. With nseg > 0 the row's range comes from the score
+// kernel (segment s's min and max in the row's selection entries 2s, 2s+1).
 __global__ void __launch_bounds__(kTopkThreads)
     topk_kernel(const float *__restrict__ scores, int64_t stride, int64_t n, int64_t offset,
-                int32_t ratio, int64_t r0, int32_t k, int32_t *__restrict__ sel) {
+                int32_t ratio, int64_t r0, int32_t k, int32_t nseg, int32_t *__restrict__ sel) {
     __shared__ uint32_t hist[kBins];
     __shared__ uint32_t cand[kCandCap];
     __shared__ int32_t cand_j[kCandCap];
@@ -419,7 +478,7 @@ __global__ void __launch_bounds__(kTopkThreads)
     __shared__ uint32_t w_gt[kTopkWarps], w_eq[kTopkWarps];
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int row = blockIdx.x;
+    const int row = static_cast<int>(gridDim.x - 1 - blockIdx.x);
     const int64_t t = offset + r0 + row;
     const int64_t L = min(n, (t + 1) / ratio);
     int32_t *out = sel + (r0 + row) * static_cast<int64_t>(k);
@@ -433,10 +492,17 @@ __global__ void __launch_bounds__(kTopkThreads)
 
     // ---- 1. range of the row
     float vmin = INFINITY, vmax = -INFINITY;
-    for (int64_t j = lo + lane; j < hi; j += 32) {
-        const float v = src[j];
-        vmin = fminf(vmin, v);
-        vmax = fmaxf(vmax, v);
+    if (nseg > 0) {
+        if (warp == 0 && lane < nseg) {
+            vmin = __int_as_float(out[2 * lane]);
+            vmax = __int_as_float(out[2 * lane + 1]);
+        }
+    } else {
+        for (int64_t j = lo + lane; j < hi; j += 32) {
+            const float v = src[j];
+            vmin = fminf(vmin, v);
+            vmax = fmaxf(vmax, v);
+        }
     }
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) {
@@ -611,7 +677,8 @@ int launch_fill_selection(int32_t *sel, int64_t rows, int32_t k, int64_t offset,
 
 int launch_score_tile(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const float *w, int64_t n,
                       int64_t offset, int32_t ratio, int64_t r0, int64_t R, float *scores,
-                      int64_t stride, int32_t *status, cudaStream_t s) {
+                      int64_t stride, int32_t *sel, int32_t k, int *nseg_rng, int32_t *status,
+                      cudaStream_t s) {
     static bool attr_set = false;
     if (!attr_set) {
         if (cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -633,6 +700,11 @@ int launch_score_tile(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const fl
     const int groups = static_cast<int>((R + kTok - 1) / kTok);
     p.nseg = choose_segments(groups, p.NB, sms);
     p.n_units = groups * p.nseg;
+    // the row ranges fit the selection rows when they hold two entries per segment
+    const bool rng = sel != nullptr && k >= 2 * p.nseg;
+    p.rng = rng ? sel : nullptr;
+    p.k = k;
+    if (nseg_rng) *nseg_rng = rng ? p.nseg : 0;
     p.status = status;
     const int grid = std::min(p.n_units, sms);
     score_kernel<<<grid, kScoreThreads, kScoreSmem, s>>>(tm_q, tm_k, p);
@@ -640,11 +712,11 @@ int launch_score_tile(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const fl
 }
 
 int launch_topk_tile(const float *scores, int64_t stride, int64_t n, int64_t offset,
-                     int32_t ratio, int64_t r0, int64_t R, int32_t k, int32_t *sel,
-                     int32_t *status, cudaStream_t s) {
+                     int32_t ratio, int64_t r0, int64_t R, int32_t k, int32_t nseg_rng,
+                     int32_t *sel, int32_t *status, cudaStream_t s) {
     (void)status;
     topk_kernel<<<static_cast<unsigned>(R), kTopkThreads, 0, s>>>(scores, stride, n, offset, ratio,
-                                                                 r0, k, sel);
+                                                                 r0, k, nseg_rng, sel);
     return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
@@ -681,10 +753,11 @@ int run_score_topk(const void *q_idx, const float *w, const void *pooled_ik, int
     float *scores = static_cast<float *>(scratch);
     for (int64_t r0 = 0; r0 < chunk; r0 += tile_rows) {
         const int64_t R = std::min(tile_rows, chunk - r0);
-        int rc =
-            launch_score_tile(tm_q, tm_k, w, n, offset, ratio, r0, R, scores, stride, status, s);
+        int nseg_rng = 0;
+        int rc = launch_score_tile(tm_q, tm_k, w, n, offset, ratio, r0, R, scores, stride, sel, k,
+                                   &nseg_rng, status, s);
         if (rc != DSA_OK) return rc;
-        rc = launch_topk_tile(scores, stride, n, offset, ratio, r0, R, k, sel, status, s);
+        rc = launch_topk_tile(scores, stride, n, offset, ratio, r0, R, k, nseg_rng, sel, status, s);
         if (rc != DSA_OK) return rc;
     }
     return DSA_OK;
