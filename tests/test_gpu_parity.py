@@ -115,6 +115,43 @@ def test_topk_ties_break_toward_lower_index(dsa):
     assert np.array_equal(sel.cpu().numpy(), oracle.topk(gpu_s, pos, n, 4, k))
 
 
+@pytest.mark.parametrize("L,m,k", [(4000, 100, 64), (4000, 600, 300), (4000, 100, 3000),
+                                   (70000, 100, 64), (70000, 3000, 2048)])
+def test_topk_heavy_ties_on_every_selection_path(dsa, L, m, k):
+    """m pooled rows are one repeated key aligned with every indexer query, so m
+    scores are exactly equal and above all others; the rest are ReLU'd random
+    dot products, about half of them exactly 0. With k < m the k-th place is
+    inside the repeated group, with k = 3000 it is inside the zeros. The cases
+    cover every way the top-k finds its threshold: a few candidates ranked
+    against each other, a crowded threshold bin (radix select over the
+    candidates), and a bin too crowded to collect (radix select over the row),
+    on rows of 4,000 and of 70,000 scores. Ties must go to the lowest indices."""
+    g = torch.Generator().manual_seed(L + m + k)
+    off, T = 4 * L, 4
+    n = (off + T) // 4
+    v = torch.randn(128, generator=g)
+    q_idx = v.expand(T, 64, 128).to(torch.bfloat16).contiguous()
+    w = torch.rand(T, 64, generator=g) * 0.125 + 0.01
+    pik = torch.randn(n, 128, generator=g)
+    dup = torch.randperm(L, generator=g)[:m]
+    pik[dup] = 8.0 * v / v.norm() * math.sqrt(128)
+    pik = pik.to(torch.bfloat16)
+    sel = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    scratch = torch.empty(B.dsa_score_scratch_bytes(T, n) // 4, dtype=torch.float32,
+                          device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.dsa_index_score_topk(q_idx.cuda(), w.cuda(), pik.cuda(), n, T, off, 4, k, T, scratch,
+                           sel, status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    stride = (n + 127) // 128 * 128
+    gpu_s = scratch[: T * stride].view(T, stride)[:, :n].cpu().numpy()
+    for r in range(T):   # the ties are real: one value over the whole repeated group
+        assert np.unique(gpu_s[r, dup.numpy()]).size == 1
+    pos = off + np.arange(T)
+    assert np.array_equal(sel.cpu().numpy(), oracle.topk(gpu_s, pos, n, 4, k))
+
+
 @pytest.mark.parametrize("tiles", [(1, 7, 64, 333), (512, 1000)])
 def test_tile_size_changes_no_index(dsa, tiles):
     off, T, k = 4096, 1000, 256
