@@ -417,6 +417,23 @@ def main():
     launches_per_step = (1 + (1 if (wl.off0 + T) % r else 0)   # pool (+ remainder)
                          + (1 if skip else 2 * n_tiles)          # fill, or score+top-k per tile
                          + 1)                                    # attention
+    if skip:
+        # nothing is scored on the skip path: a selection fill only
+        st_roof = {"kernel": "fill_selection_kernel (dsa_index_score_topk skip path: every "
+                             "pooled row fits in index_topk)",
+                   "bound": None, "frac": None, "ms_per_call": comp_ms["score_topk"]}
+    else:
+        # the fused indexer step: score kernel + top-k kernel of each tile
+        st_traffic = ncu_traffic("score_kernel", args.workload)
+        if st_traffic is not None:
+            st_traffic += ncu_traffic("topk_kernel", args.workload)
+        st_roof = {"kernel": "score_kernel + topk_kernel (dsa_index_score_topk)",
+                   "bound": "tensor", "achieved": st_tf, "peak": peak_tf, "unit": "TFLOP/s",
+                   "frac": st_tf / peak_tf, "traffic": st_traffic,
+                   "peak_source": f"{src} bf16 dense (burst)",
+                   "algorithmic_flops_per_launch": counts["score_flops"],
+                   "ms_per_call": comp_ms["score_topk"],
+                   "topk_algorithmic_bytes": counts["topk_bytes"], "hbm_peak_gbs": peak_bw}
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
@@ -435,18 +452,7 @@ def main():
                      "peak_source": f"{src} bf16 dense (burst)",
                      "algorithmic_flops_per_launch": counts["attn_flops"],
                      "ms_per_launch": comp_ms["attention"]},
-        # the fused indexer step: score kernel + top-k kernel of each tile
-        "score_topk_roofline": {"kernel": "score_kernel + topk_kernel (dsa_index_score_topk)",
-                                "bound": "tensor", "achieved": st_tf, "peak": peak_tf,
-                                "unit": "TFLOP/s", "frac": st_tf / peak_tf,
-                                "traffic": (None if ncu_traffic("score_kernel", args.workload) is None
-                                            else ncu_traffic("score_kernel", args.workload)
-                                            + ncu_traffic("topk_kernel", args.workload)),
-                                "peak_source": f"{src} bf16 dense (burst)",
-                                "algorithmic_flops_per_launch": counts["score_flops"],
-                                "ms_per_call": comp_ms["score_topk"],
-                                "topk_algorithmic_bytes": counts["topk_bytes"],
-                                "hbm_peak_gbs": peak_bw},
+        "score_topk_roofline": st_roof,
         "components_ms": comp_ms,
         "gpu_launches": args.steps * launches_per_step,
         "clocks": clk.summary(),

@@ -10,6 +10,11 @@
 // Arithmetic: a pooled element is the mean of `ratio` bf16 values (a power of
 // two up to 128: the fp64 sum, taken in row order, is exact for such values in
 // practice, and /ratio is exact), rounded once to bf16 with ties to even.
+// GB300's fp64 rate is a small fraction of its fp32 rate, so the sum is first
+// taken in fp32 with an error-free check of every addition (TwoSum); only when
+// some fp32 partial sum rounded is it taken again in fp64. While every fp32
+// partial sum is exact, the fp64 partial sums are the same values, so the
+// result is the fp64 row-order sum either way.
 // HBM-bound: each thread moves one 16-byte vector of each of the raw rows and
 // writes one 16-byte vector of the pooled row.
 #include <cudaTypedefs.h>
@@ -46,11 +51,32 @@ __device__ __forceinline__ uint32_t bf16_rne_from_double(double x) {
     return sign | (r >= 0x7F80u ? 0x7F80u : r);
 }
 
-__device__ __forceinline__ void add8(double (&acc)[8], uint4 x) {
-    acc[0] += bf16lo(x.x); acc[1] += bf16hi(x.x);
-    acc[2] += bf16lo(x.y); acc[3] += bf16hi(x.y);
-    acc[4] += bf16lo(x.z); acc[5] += bf16hi(x.z);
-    acc[6] += bf16lo(x.w); acc[7] += bf16hi(x.w);
+// a + b rounded to fp32; sets `bit` in `inexact` when that rounding lost
+// anything (Knuth's TwoSum: s + err == a + b exactly; an infinity or NaN gives
+// err NaN).
+__device__ __forceinline__ float add_checked(float a, float b, uint32_t &inexact, uint32_t bit) {
+    const float s = __fadd_rn(a, b);
+    const float bb = __fsub_rn(s, a);
+    const float err = __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb));
+    if (!(err == 0.0f)) inexact |= bit;
+    return s;
+}
+
+__device__ __forceinline__ void add8_checked(float (&acc)[8], uint4 x, uint32_t &inexact) {
+    acc[0] = add_checked(acc[0], bf16lo(x.x), inexact, 1u);
+    acc[1] = add_checked(acc[1], bf16hi(x.x), inexact, 2u);
+    acc[2] = add_checked(acc[2], bf16lo(x.y), inexact, 4u);
+    acc[3] = add_checked(acc[3], bf16hi(x.y), inexact, 8u);
+    acc[4] = add_checked(acc[4], bf16lo(x.z), inexact, 16u);
+    acc[5] = add_checked(acc[5], bf16hi(x.z), inexact, 32u);
+    acc[6] = add_checked(acc[6], bf16lo(x.w), inexact, 64u);
+    acc[7] = add_checked(acc[7], bf16hi(x.w), inexact, 128u);
+}
+
+// Element e (0..7) of a 16-byte vector of bf16 values.
+__device__ __forceinline__ float elem8(uint4 x, int e) {
+    const uint32_t w = e < 2 ? x.x : e < 4 ? x.y : e < 6 ? x.z : x.w;
+    return (e & 1) ? bf16hi(w) : bf16lo(w);
 }
 
 // One thread per (new pooled row, 16-byte vector): 64 vectors of KV then 16
@@ -74,17 +100,48 @@ __global__ void __launch_bounds__(256) pool_kernel(const uint4 *__restrict__ raw
     const uint4 *rem = is_kv ? rem_kv : rem_ik;
     const int64_t rem_base = n_old * ratio;  // absolute token held in remainder slot 0
 
-    double acc[8] = {0, 0, 0, 0, 0, 0, 0, 0};
-#pragma unroll 4
-    for (int i = 0; i < ratio; ++i) {
+    auto row = [&](int i) {
         const int64_t u = g * ratio + i;
-        const uint4 x = (u < offset) ? rem[(u - rem_base) * per_row + vv]
-                                     : __ldg(&raw[(u - offset) * per_row + vv]);
-        add8(acc, x);
+        return (u < offset) ? rem[(u - rem_base) * per_row + vv]
+                            : __ldg(&raw[(u - offset) * per_row + vv]);
+    };
+    // rows are loaded kBatch at a time, all in flight before any is summed
+    constexpr int kBatch = 8;
+    float acc32[8] = {0, 0, 0, 0, 0, 0, 0, 0};
+    uint32_t inexact = 0;  // bit e: element e's fp32 running sum rounded somewhere
+    for (int i0 = 0; i0 < ratio; i0 += kBatch) {
+        uint4 x[kBatch];
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j)
+            if (i0 + j < ratio) x[j] = row(i0 + j);
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j)
+            if (i0 + j < ratio) add8_checked(acc32, x[j], inexact);
+    }
+    double acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = acc32[e];
+    // only the elements whose fp32 sum rounded are summed again, in fp64
+    while (inexact) {
+        const int e = __ffs(inexact) - 1;
+        inexact &= inexact - 1;
+        double a = 0.0;
+        for (int i0 = 0; i0 < ratio; i0 += kBatch) {
+            float y[kBatch];
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j)
+                if (i0 + j < ratio) y[j] = elem8(row(i0 + j), e);
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j)
+                if (i0 + j < ratio) a += y[j];
+        }
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            if (k == e) acc[k] = a;  // (a static index keeps acc in registers)
     }
     uint32_t o[8];
-#pragma unroll
     const double inv = 1.0 / ratio;  // exact: ratio is a power of two
+#pragma unroll
     for (int e = 0; e < 8; ++e) o[e] = bf16_rne_from_double(acc[e] * inv);
     uint4 out;
     out.x = o[0] | (o[1] << 16);
@@ -92,6 +149,75 @@ __global__ void __launch_bounds__(256) pool_kernel(const uint4 *__restrict__ raw
     out.z = o[4] | (o[5] << 16);
     out.w = o[6] | (o[7] << 16);
     (is_kv ? pooled_kv : pooled_ik)[g * per_row + vv] = out;
+}
+
+constexpr int kWordKV = kD / 2;   // 256 4-byte words (bf16 pairs) per KV row
+constexpr int kWordIK = kDI / 2;  // 64 per indexer-key row
+constexpr int kWordRow = kWordKV + kWordIK;
+
+// The same mean for large ratios: one thread per (new pooled row, 4-byte
+// word), so that a thread keeps 32 raw rows in flight rather than 8 (with
+// `ratio` rows to sum, a thread is bound by its chain of loads).
+__global__ void __launch_bounds__(256) pool_words_kernel(const uint32_t *__restrict__ raw_kv,
+                                                         const uint32_t *__restrict__ raw_ik,
+                                                         const uint32_t *__restrict__ rem_kv,
+                                                         const uint32_t *__restrict__ rem_ik,
+                                                         uint32_t *__restrict__ pooled_kv,
+                                                         uint32_t *__restrict__ pooled_ik,
+                                                         int64_t n_old, int64_t n_new,
+                                                         int64_t offset, int32_t ratio) {
+    const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (idx >= (n_new - n_old) * kWordRow) return;
+    const int64_t g = n_old + idx / kWordRow;
+    const int v = static_cast<int>(idx % kWordRow);
+    const bool is_kv = v < kWordKV;
+    const int vv = is_kv ? v : v - kWordKV;
+    const int per_row = is_kv ? kWordKV : kWordIK;
+    const uint32_t *raw = is_kv ? raw_kv : raw_ik;
+    const uint32_t *rem = is_kv ? rem_kv : rem_ik;
+    // row i of the group: remainder slot or chunk row (one pointer step per row)
+    const int64_t u0 = g * ratio;
+    const uint32_t *rem_p = rem + (u0 - n_old * ratio) * per_row + vv;
+    const uint32_t *raw_p = raw + (u0 - offset) * per_row + vv;
+    auto row = [&](int i) {
+        return (u0 + i < offset) ? rem_p[i * per_row] : __ldg(raw_p + i * per_row);
+    };
+    constexpr int kBatch = 32;
+    float a0 = 0.0f, a1 = 0.0f;
+    uint32_t inexact = 0;
+    for (int i0 = 0; i0 < ratio; i0 += kBatch) {
+        uint32_t x[kBatch];
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j)
+            if (i0 + j < ratio) x[j] = row(i0 + j);
+#pragma unroll
+        for (int j = 0; j < kBatch; ++j)
+            if (i0 + j < ratio) {
+                a0 = add_checked(a0, bf16lo(x[j]), inexact, 1u);
+                a1 = add_checked(a1, bf16hi(x[j]), inexact, 2u);
+            }
+    }
+    double d0 = a0, d1 = a1;
+    if (inexact) {
+        // some fp32 partial sum rounded: both sums again in fp64, in row order
+        d0 = 0.0;
+        d1 = 0.0;
+        for (int i0 = 0; i0 < ratio; i0 += kBatch) {
+            uint32_t x[kBatch];
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j)
+                if (i0 + j < ratio) x[j] = row(i0 + j);
+#pragma unroll
+            for (int j = 0; j < kBatch; ++j)
+                if (i0 + j < ratio) {
+                    d0 += bf16lo(x[j]);
+                    d1 += bf16hi(x[j]);
+                }
+        }
+    }
+    const double inv = 1.0 / ratio;  // exact: ratio is a power of two
+    (is_kv ? pooled_kv : pooled_ik)[g * per_row + vv] =
+        bf16_rne_from_double(d0 * inv) | (bf16_rne_from_double(d1 * inv) << 16);
 }
 
 // Copy the chunk rows that form the new remainder (tokens 4*n_new .. end-1
@@ -123,13 +249,24 @@ int launch_pool_append(const dsa_pool_state &st, const void *raw_kv, const void 
     const int64_t end = offset + chunk;
     const int64_t n_new = end / ratio;
     if (n_new > n_old) {
-        const int64_t threads = (n_new - n_old) * kVecRow;
-        const int64_t blocks = (threads + 255) / 256;
-        pool_kernel<<<static_cast<unsigned>(blocks), 256, 0, s>>>(
-            static_cast<const uint4 *>(raw_kv), static_cast<const uint4 *>(raw_ik),
-            static_cast<const uint4 *>(st.rem_kv), static_cast<const uint4 *>(st.rem_ik),
-            static_cast<uint4 *>(st.pooled_kv), static_cast<uint4 *>(st.pooled_ik), n_old, n_new,
-            offset, ratio);
+        // large ratios: a thread per 4-byte word; few new rows: smaller blocks
+        // spread them over more SMs
+        const bool words = ratio >= 32;
+        const int64_t threads = (n_new - n_old) * (words ? kWordRow : kVecRow);
+        const int bs = (threads + 255) / 256 >= 2 * static_cast<int64_t>(sm_count()) ? 256 : 64;
+        const int64_t blocks = (threads + bs - 1) / bs;
+        if (words)
+            pool_words_kernel<<<static_cast<unsigned>(blocks), bs, 0, s>>>(
+                static_cast<const uint32_t *>(raw_kv), static_cast<const uint32_t *>(raw_ik),
+                static_cast<const uint32_t *>(st.rem_kv), static_cast<const uint32_t *>(st.rem_ik),
+                static_cast<uint32_t *>(st.pooled_kv), static_cast<uint32_t *>(st.pooled_ik),
+                n_old, n_new, offset, ratio);
+        else
+            pool_kernel<<<static_cast<unsigned>(blocks), bs, 0, s>>>(
+                static_cast<const uint4 *>(raw_kv), static_cast<const uint4 *>(raw_ik),
+                static_cast<const uint4 *>(st.rem_kv), static_cast<const uint4 *>(st.rem_ik),
+                static_cast<uint4 *>(st.pooled_kv), static_cast<uint4 *>(st.pooled_ik), n_old,
+                n_new, offset, ratio);
         if (cudaGetLastError() != cudaSuccess) return DSA_ERR_CUDA;
     }
     if (end % ratio != 0) {

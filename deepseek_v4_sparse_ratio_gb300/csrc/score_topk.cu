@@ -370,8 +370,10 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 
 // ------------------------------------------------------------------ top-k kernel
 
+// threads per top-k CTA: 256 (several CTAs per SM) when the tile has rows
+// enough to fill the GPU, else 1024, so a few rows walk their scores 4x faster
 constexpr int kTopkThreads = 256;
-constexpr int kTopkWarps = kTopkThreads / 32;
+constexpr int kTopkThreadsFew = 1024;
 constexpr int kBins = 2048;
 constexpr int kCandCap = 2048;
 
@@ -381,6 +383,7 @@ __device__ __forceinline__ uint32_t order_key(float f) {
 }
 
 // Exclusive block-wide prefix sum of a per-thread value; *total gets the sum.
+template <int NT>
 __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *warp_sums,
                                                     uint32_t *total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -393,33 +396,34 @@ __device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *warp_s
     if (lane == 31) warp_sums[warp] = inc;
     __syncthreads();
     if (warp == 0) {
-        uint32_t x = lane < kTopkWarps ? warp_sums[lane] : 0;
+        uint32_t x = lane < (NT / 32) ? warp_sums[lane] : 0;
         uint32_t xi = x;
 #pragma unroll
         for (int o = 1; o < 32; o <<= 1) {
             const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, xi, o);
             if (lane >= o) xi += y;
         }
-        if (lane < kTopkWarps) warp_sums[lane] = xi - x;
-        if (lane == kTopkWarps - 1) warp_sums[kTopkWarps] = xi;
+        if (lane < (NT / 32)) warp_sums[lane] = xi - x;
+        if (lane == (NT / 32) - 1) warp_sums[(NT / 32)] = xi;
     }
     __syncthreads();
     const uint32_t r = warp_sums[warp] + inc - v;
-    *total = warp_sums[kTopkWarps];
+    *total = warp_sums[(NT / 32)];
     __syncthreads();
     return r;
 }
 
 // After hist[0..nb) is filled: the bin b holding the `need`-th largest element
 // (counting from the top bin down) and how many elements lie in higher bins.
+template <int NT>
 __device__ __forceinline__ void find_bin(const uint32_t *hist, int nb, uint32_t need,
                                          uint32_t *warp_sums, uint32_t *s_bin, uint32_t *s_above) {
-    const int per = nb / kTopkThreads;
+    const int per = nb / NT;
     const int top = nb - per * threadIdx.x;  // thread i owns bins [top-per, top)
     uint32_t mine = 0;
     for (int b = top - per; b < top; ++b) mine += hist[b];
     uint32_t tot;
-    uint32_t cum = block_excl_scan(mine, warp_sums, &tot);
+    uint32_t cum = block_excl_scan<NT>(mine, warp_sums, &tot);
     for (int b = top - 1; b >= top - per; --b) {
         const uint32_t c = hist[b];
         if (cum < need && need <= cum + c) {
@@ -434,7 +438,7 @@ __device__ __forceinline__ void find_bin(const uint32_t *hist, int nb, uint32_t 
 // Radix select over `count` order keys given by key_at(i): the key of the
 // need-th largest element and how many elements equal to it are kept
 // (11/11/10-bit digits from the top).
-template <typename KeyAt>
+template <int NT, typename KeyAt>
 __device__ __forceinline__ void radix_select(KeyAt key_at, int64_t count, uint32_t need,
                                              uint32_t *hist, uint32_t *warp_sums, uint32_t *s_bin,
                                              uint32_t *s_above, uint32_t *thr_out,
@@ -444,15 +448,15 @@ __device__ __forceinline__ void radix_select(KeyAt key_at, int64_t count, uint32
         const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
         const int bits = pass == 2 ? 10 : 11;
         const int nb = 1 << bits;
-        for (int i = threadIdx.x; i < nb; i += kTopkThreads) hist[i] = 0;
+        for (int i = threadIdx.x; i < nb; i += NT) hist[i] = 0;
         __syncthreads();
-        for (int64_t j = threadIdx.x; j < count; j += kTopkThreads) {
+        for (int64_t j = threadIdx.x; j < count; j += NT) {
             const uint32_t u = key_at(j);
             if (pass == 0 || (u >> (shift + bits)) == prefix)
                 atomicAdd(&hist[(u >> shift) & (nb - 1)], 1u);
         }
         __syncthreads();
-        find_bin(hist, nb, need, warp_sums, s_bin, s_above);
+        find_bin<NT>(hist, nb, need, warp_sums, s_bin, s_above);
         prefix = (prefix << bits) | *s_bin;
         need -= *s_above;
         __syncthreads();
@@ -466,16 +470,17 @@ __device__ __forceinline__ void radix_select(KeyAt key_at, int64_t count, uint32
 // taken last first: the score kernel writes the last rows last, so theirs are
 // the scores still in L2. With nseg > 0 the row's range comes from the score
 // kernel (segment s's min and max in the row's selection entries 2s, 2s+1).
-__global__ void __launch_bounds__(kTopkThreads)
+template <int NT>
+__global__ void __launch_bounds__(NT)
     topk_kernel(const float *__restrict__ scores, int64_t stride, int64_t n, int64_t offset,
                 int32_t ratio, int64_t r0, int32_t k, int32_t nseg, int32_t *__restrict__ sel) {
     __shared__ uint32_t hist[kBins];
     __shared__ uint32_t cand[kCandCap];
     __shared__ int32_t cand_j[kCandCap];
-    __shared__ uint32_t warp_sums[kTopkWarps + 1];
+    __shared__ uint32_t warp_sums[(NT / 32) + 1];
     __shared__ uint32_t s_bin, s_above, s_cnt;
-    __shared__ float s_min[kTopkWarps], s_max[kTopkWarps];
-    __shared__ uint32_t w_gt[kTopkWarps], w_eq[kTopkWarps];
+    __shared__ float s_min[(NT / 32)], s_max[(NT / 32)];
+    __shared__ uint32_t w_gt[(NT / 32)], w_eq[(NT / 32)];
 
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int row = static_cast<int>(gridDim.x - 1 - blockIdx.x);
@@ -483,11 +488,11 @@ __global__ void __launch_bounds__(kTopkThreads)
     const int64_t L = min(n, (t + 1) / ratio);
     int32_t *out = sel + (r0 + row) * static_cast<int64_t>(k);
     if (L <= k) {
-        for (int i = threadIdx.x; i < k; i += kTopkThreads) out[i] = i < L ? i : -1;
+        for (int i = threadIdx.x; i < k; i += NT) out[i] = i < L ? i : -1;
         return;
     }
     const float *src = scores + static_cast<int64_t>(row) * stride;
-    const int64_t seg = ((L + kTopkWarps - 1) / kTopkWarps + 31) / 32 * 32;
+    const int64_t seg = ((L + (NT / 32) - 1) / (NT / 32) + 31) / 32 * 32;
     const int64_t lo = min(L, seg * warp), hi = min(L, seg * (warp + 1));
 
     // ---- 1. range of the row
@@ -513,13 +518,13 @@ __global__ void __launch_bounds__(kTopkThreads)
         s_min[warp] = vmin;
         s_max[warp] = vmax;
     }
-    for (int i = threadIdx.x; i < kBins; i += kTopkThreads) hist[i] = 0;
+    for (int i = threadIdx.x; i < kBins; i += NT) hist[i] = 0;
     if (threadIdx.x == 0) s_cnt = 0;
     __syncthreads();
     vmin = s_min[0];
     vmax = s_max[0];
 #pragma unroll
-    for (int w = 1; w < kTopkWarps; ++w) {
+    for (int w = 1; w < (NT / 32); ++w) {
         vmin = fminf(vmin, s_min[w]);
         vmax = fmaxf(vmax, s_max[w]);
     }
@@ -537,7 +542,7 @@ __global__ void __launch_bounds__(kTopkThreads)
         auto bin_of = [&](float v) { return min(kBins - 1, static_cast<int>((v - vmin) * scale)); };
         for (int64_t j = lo + lane; j < hi; j += 32) atomicAdd(&hist[bin_of(src[j])], 1u);
         __syncthreads();
-        find_bin(hist, kBins, static_cast<uint32_t>(k), warp_sums, &s_bin, &s_above);
+        find_bin<NT>(hist, kBins, static_cast<uint32_t>(k), warp_sums, &s_bin, &s_above);
         const int bstar = static_cast<int>(s_bin);
         const uint32_t need = static_cast<uint32_t>(k) - s_above;
         // ---- 3. the threshold bin's elements are the candidates; count each
@@ -563,7 +568,7 @@ __global__ void __launch_bounds__(kTopkThreads)
         }
         __syncthreads();
         const uint32_t cnt = s_cnt;
-        if (cnt <= kTopkThreads) {
+        if (cnt <= NT) {
             // few candidates (the usual case: one linear bin near the threshold holds a
             // handful of scores): each thread ranks one candidate against all of them;
             // the need-th largest has fewer than `need` strictly larger keys and at
@@ -585,12 +590,12 @@ __global__ void __launch_bounds__(kTopkThreads)
             thr = s_bin;
             need_eq = s_above;
         } else if (cnt <= kCandCap) {
-            radix_select([&](int64_t c) { return cand[c]; }, cnt, need, hist, warp_sums, &s_bin,
+            radix_select<NT>([&](int64_t c) { return cand[c]; }, cnt, need, hist, warp_sums, &s_bin,
                          &s_above, &thr, &need_eq);
         }
         if (cnt <= kCandCap) {
             // candidates above / equal to the threshold, by segment
-            for (uint32_t c = threadIdx.x; c < cnt; c += kTopkThreads) {
+            for (uint32_t c = threadIdx.x; c < cnt; c += NT) {
                 const int w = static_cast<int>(cand_j[c] / seg);
                 if (cand[c] > thr) atomicAdd(&w_gt[w], 1u);
                 else if (cand[c] == thr) atomicAdd(&w_eq[w], 1u);
@@ -598,7 +603,7 @@ __global__ void __launch_bounds__(kTopkThreads)
             __syncthreads();
             counted = true;
         } else {
-            radix_select([&](int64_t j) { return order_key(src[j]); }, L, static_cast<uint32_t>(k),
+            radix_select<NT>([&](int64_t j) { return order_key(src[j]); }, L, static_cast<uint32_t>(k),
                          hist, warp_sums, &s_bin, &s_above, &thr, &need_eq);
         }
     }
@@ -715,8 +720,12 @@ int launch_topk_tile(const float *scores, int64_t stride, int64_t n, int64_t off
                      int32_t ratio, int64_t r0, int64_t R, int32_t k, int32_t nseg_rng,
                      int32_t *sel, int32_t *status, cudaStream_t s) {
     (void)status;
-    topk_kernel<<<static_cast<unsigned>(R), kTopkThreads, 0, s>>>(scores, stride, n, offset, ratio,
-                                                                 r0, k, nseg_rng, sel);
+    if (R < 2 * static_cast<int64_t>(sm_count()))
+        topk_kernel<kTopkThreadsFew><<<static_cast<unsigned>(R), kTopkThreadsFew, 0, s>>>(
+            scores, stride, n, offset, ratio, r0, k, nseg_rng, sel);
+    else
+        topk_kernel<kTopkThreads><<<static_cast<unsigned>(R), kTopkThreads, 0, s>>>(
+            scores, stride, n, offset, ratio, r0, k, nseg_rng, sel);
     return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 

@@ -90,7 +90,7 @@ def draw(w: Workload) -> Workload:
 
 
 def workload(name: str) -> Workload:
-    """The five named workloads (without tensors; call ``draw``)."""
+    """A named workload (without tensors; call ``draw``)."""
     if name == "zero_prefix_512":
         return Workload(name, 0, [512], 0, 0, index_topk=64, window=128,
                         tile_rows=(512, 192))
@@ -117,11 +117,21 @@ def workload(name: str) -> Workload:
         off = 131072 - 4096
         return Workload(name, 6, [4096], off, off // 128, index_topk=1024, window=128,
                         ratio=128, sample_rows=128, tile_rows=(4096,))
+    # the short shapes: an exact 4-row band and a single-row decode step at 128K
+    if name == "band_128k":
+        off = 131072 - 4
+        return Workload(name, 7, [4], off, off // RATIO, index_topk=2048, window=128,
+                        tile_rows=(4,))
+    if name == "decode_128k":
+        off = 131072 - 4
+        return Workload(name, 8, [1], off, off // RATIO, index_topk=2048, window=128,
+                        tile_rows=(1,))
     raise KeyError(name)
 
 
 WORKLOADS = ("zero_prefix_512", "two_chunks_4098", "prompt_16k", "ctx_128k", "ctx_1m")
 COMPRESSED_WORKLOADS = ("compressed_16k", "compressed_128k")
+SHORT_WORKLOADS = ("band_128k", "decode_128k")
 
 
 def small(seed: int, chunks, index_topk: int, window: int = 128, off0: int = 0,

@@ -89,6 +89,14 @@ def test_window_only_local_attention_at_long_offset(dsa):
     check_attention(bf16_to_f64(out), ref)
 
 
+@pytest.mark.parametrize("name", inputs.SHORT_WORKLOADS)
+def test_short_shapes_at_128k_parity(dsa, name):
+    """A 4-row band and a 1-row decode step over a 32,767-row pooled prefix: the
+    full score + top-k path (n > index_topk) on every row."""
+    wl = inputs.draw(inputs.workload(name))
+    run_workload_parity(wl, wl.tile_rows[0], 0)
+
+
 def test_single_token_decode_steps_after_prefill(dsa):
     """A 1000-token prefill, then eight one-token steps (the decode shape)."""
     chunks = [1000] + [1] * 8

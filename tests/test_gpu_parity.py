@@ -48,6 +48,38 @@ def test_pool_append_bitexact(dsa, chunks):
     assert np.array_equal(_bits(st.rem_ik[:ref.n_rem]), ref.rem_ik)
 
 
+@pytest.mark.parametrize("ratio", [4, 128])
+def test_pool_sum_where_fp32_rounds(dsa, ratio):
+    """Columns whose running sum is not exact in fp32: 2^10, then 2^-20, then
+    -2^10 (+ zeros) has the exact mean 2^-20 / ratio, but an fp32 running sum
+    loses the 2^-20. Other columns mix in random rows. The pooled rows must
+    still equal the oracle's exact row-order sum bit for bit."""
+    T = 2 * ratio
+    g = torch.Generator().manual_seed(ratio)
+    kv = torch.randn(T, 512, generator=g)
+    ik = torch.randn(T, 128, generator=g)
+    for x in (kv, ik):
+        cols = x[:, ::3]
+        cols[0::ratio] = 2.0 ** 10
+        cols[1::ratio] = 2.0 ** -20
+        cols[2::ratio] = -(2.0 ** 10)
+        cols[3::ratio] = 0.0
+    kv, ik = kv.to(torch.bfloat16), ik.to(torch.bfloat16)
+    st = B.PoolState(4, ratio=ratio)
+    B.dsa_pool_append(st, kv.cuda(), ik.cuda(), T, 0)
+    torch.cuda.synchronize()
+    ref = oracle.PoolState(ratio)
+    ref.append(ik, kv, 0)
+    assert st.n_pooled == ref.n_pooled == 2
+    got = _bits(st.pooled_kv[:2])
+    assert np.array_equal(got, ref.pooled_kv)
+    assert np.array_equal(_bits(st.pooled_ik[:2]), ref.pooled_ik)
+    # the exact mean survived (an fp32 running sum would give 0 here)
+    mean = torch.tensor(2.0 ** -20 / ratio).to(torch.bfloat16).view(torch.int16).item() & 0xFFFF
+    if ratio == 4:
+        assert got[0, 0] == mean
+
+
 def test_pool_ten_tokens_then_resume(dsa):
     """The pages' example: 10 tokens -> 2 pooled rows + 2 remainder; then resume."""
     wl = inputs.draw(inputs.small(3, [10, 6], index_topk=64))
@@ -115,9 +147,11 @@ def test_topk_ties_break_toward_lower_index(dsa):
     assert np.array_equal(sel.cpu().numpy(), oracle.topk(gpu_s, pos, n, 4, k))
 
 
-@pytest.mark.parametrize("L,m,k", [(4000, 100, 64), (4000, 600, 300), (4000, 100, 3000),
-                                   (70000, 100, 64), (70000, 3000, 2048)])
-def test_topk_heavy_ties_on_every_selection_path(dsa, L, m, k):
+@pytest.mark.parametrize("L,m,k,T", [(4000, 100, 64, 4), (4000, 100, 64, 320),
+                                     (4000, 600, 300, 4), (4000, 600, 300, 320),
+                                     (4000, 100, 3000, 320), (70000, 100, 64, 320),
+                                     (70000, 3000, 2048, 4)])
+def test_topk_heavy_ties_on_every_selection_path(dsa, L, m, k, T):
     """m pooled rows are one repeated key aligned with every indexer query, so m
     scores are exactly equal and above all others; the rest are ReLU'd random
     dot products, about half of them exactly 0. With k < m the k-th place is
@@ -125,9 +159,11 @@ def test_topk_heavy_ties_on_every_selection_path(dsa, L, m, k):
     cover every way the top-k finds its threshold: a few candidates ranked
     against each other, a crowded threshold bin (radix select over the
     candidates), and a bin too crowded to collect (radix select over the row),
-    on rows of 4,000 and of 70,000 scores. Ties must go to the lowest indices."""
+    on rows of 4,000 and of 70,000 scores, in tiles of 4 rows (1024-thread
+    CTAs) and of 320 rows (256-thread CTAs). Ties must go to the lowest
+    indices."""
     g = torch.Generator().manual_seed(L + m + k)
-    off, T = 4 * L, 4
+    off = 4 * L
     n = (off + T) // 4
     v = torch.randn(128, generator=g)
     q_idx = v.expand(T, 64, 128).to(torch.bfloat16).contiguous()

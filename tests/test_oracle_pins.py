@@ -130,7 +130,7 @@ def test_offset_mismatch_is_rejected():
         st.append(_bf16((3, 128), 1), _bf16((3, 512), 2), 4)
 
 
-@pytest.mark.parametrize("name", inputs.WORKLOADS)
+@pytest.mark.parametrize("name", inputs.WORKLOADS + inputs.SHORT_WORKLOADS)
 def test_workload_cache_states_closed_form(name):
     """Pooled rows after each chunk: floor(tokens/4); remainder tokens mod 4."""
     wl = inputs.workload(name)
@@ -149,6 +149,8 @@ def test_workload_cache_states_closed_form(name):
         "prompt_16k": [(512 * c, 0) for c in range(1, 9)],
         "ctx_128k": [(32768, 0)],
         "ctx_1m": [(262144, 0)],
+        "band_128k": [(32768, 0)],       # 131,068 + 4 tokens
+        "decode_128k": [(32767, 1)],     # 131,068 + 1 token: one raw row left over
     }[name]
     assert got == expect
 
