@@ -229,7 +229,7 @@ def run_reference(args):
     import numpy as np
     import oracle
     from deepseek_v4_sparse_ratio_gb300 import inputs
-    wl = inputs.draw(inputs.workload(WORKLOAD))
+    wl = inputs.draw(inputs.workload(args.workload))
     T, off = wl.chunks[0], wl.off0
     oracle.build()
     base = oracle.PoolState.from_prefix(wl.t["prefix_ik"], wl.t["prefix_kv"], off, wl.ratio)
@@ -255,18 +255,33 @@ def run_reference(args):
         step(args.warmup + i)
     dt = (time.perf_counter() - t0) / args.steps
     value = rows_per_step / dt
-    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": 0,
+    cfg = run_config(wl, args.workload, args.tile_rows or wl.tile_rows[0], args.gpus)
+    cfg["reference"] = (f"the CPU oracle on the host cores of rank 0, {rows_per_step} sampled "
+                        f"query rows per step")
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": UNIT,
+            "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic",
-            "config": {"workload": WORKLOAD_DESC, "rows_per_step": rows_per_step},
+            "config": cfg,
             "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.threads(),
                              "kind": "oracle",
-                             "sample": f"{rows_per_step} query rows per step (of 4096) + the "
+                             "sample": f"{rows_per_step} query rows per step (of {T}) + the "
                                        f"chunk's pooling"},
             "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+def run_config(wl, name, tile, world):
+    """The `config` object of both arms' JSON lines."""
+    T = wl.chunks[0]
+    return {"workload": WORKLOAD_DESC if name == WORKLOAD else name,
+            "name": wl.name, "chunk": T, "context": wl.end, "ratio": wl.ratio,
+            "index_topk": wl.index_topk, "tile_rows": tile,
+            "pooled_rows": (wl.off0 + T) // wl.ratio,
+            "l2": "flushed between steps (512 MiB write, outside the step events)",
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
 
 
 def main():
@@ -438,11 +453,7 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": WORKLOAD_DESC if args.workload == WORKLOAD else args.workload,
-                   "name": wl.name, "chunk": T, "context": wl.end, "ratio": r,
-                   "index_topk": wl.index_topk, "tile_rows": tile, "pooled_rows": n,
-                   "l2": "flushed between steps (512 MiB write, outside the step events)",
-                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "config": run_config(wl, args.workload, tile, world),
         # the dominant kernel of the step (about half of its time): window + selected
         # attention, one attn_kernel launch per dsa_window_sparse_attn call
         "roofline": {"kernel": "attn_kernel (dsa_window_sparse_attn)", "bound": "tensor",
