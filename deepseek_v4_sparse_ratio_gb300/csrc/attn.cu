@@ -178,6 +178,49 @@ __device__ __forceinline__ void mma_commit_if(uint64_t *bar, uint32_t issue) {
         : "memory");
 }
 
+// Thread-block cluster helpers (the split mode below).
+__device__ __forceinline__ uint32_t cluster_rank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Address of the same shared-memory location in cluster CTA `rank`.
+__device__ __forceinline__ uint32_t peer_addr(uint32_t local, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(local), "r"(rank));
+    return r;
+}
+
+__device__ __forceinline__ float ld_peer(uint32_t addr) {
+    float v;
+    asm volatile("ld.shared::cluster.f32 %0, [%1];" : "=f"(v) : "r"(addr) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ float4 ld_peer4(uint32_t addr) {
+    float4 v;
+    asm volatile("ld.shared::cluster.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                 : "r"(addr)
+                 : "memory");
+    return v;
+}
+
+// Whether key block b is the last one this CTA takes of a token with nb blocks.
+template <int kSplit>
+__device__ __forceinline__ bool last_block(int b, int nb) {
+    if constexpr (kSplit == 1) return b == nb - 1;
+    else return b + kSplit >= nb;
+}
+
+// Every thread of every CTA of the cluster; orders shared-memory writes before it
+// with reads after it, in any CTA of the cluster.
+__device__ __forceinline__ void cluster_sync() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;"
+                 ::: "memory");
+}
+
 __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
     const uint32_t b = smem_u32(bar);
     const long long t0 = clock64();
@@ -185,6 +228,11 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
         if (clock64() - t0 > kWaitBudget) break;
 }
 
+// kSplit = 1: one CTA per token (persistent over tokens). kSplit > 1 (few tokens):
+// a cluster of kSplit CTAs per token, CTA r taking the token's key blocks r,
+// r + kSplit, ... with an online softmax of its own; at the token's end the
+// cluster merges the partial results through distributed shared memory.
+template <int kSplit>
 __global__ void __launch_bounds__(kAttnThreads, 1)
     attn_kernel(const __grid_constant__ CUtensorMap tm_q, const AttnParams p) {
     extern __shared__ uint8_t smem_raw[];
@@ -215,6 +263,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
     volatile int *abort_flag = reinterpret_cast<volatile int *>(tmem_holder + 1);
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    // Each role walks tokens i0, i0 + istep, ... and of each the key blocks crank,
+    // crank + kSplit, ... (read from special registers inside the roles, which keeps
+    // them out of the register budget of the narrow warps).
+#define DSA_SPLIT_COORDS                                                             \
+    const int crank = kSplit > 1 ? static_cast<int>(cluster_rank()) : 0;             \
+    const int i0 = static_cast<int>(blockIdx.x) / kSplit;                            \
+    const int istep = static_cast<int>(gridDim.x) / kSplit;
     if (threadIdx.x == 0) {
         mbar_init(q_full, 1);
         mbar_init(q_free, 1);
@@ -250,6 +305,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // lanes per 128-byte row piece, written straight into the 128-byte-swizzled tile.
         // Loader lw copies the 4-row groups lw, lw+7, lw+14, ... (at most 5, 20 rows).
         // Each block's selection entries are read one block ahead.
+        DSA_SPLIT_COORDS
         const int lw = warp;
         const uint64_t pol_stream = policy_evict_first();
         const uint32_t kv_base = smem_u32(sKV);
@@ -276,10 +332,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         };
         int tok = 0, g = 0, last_q = -1;
         bool ok = true;
-        int i = blockIdx.x;
+        int i = i0;
         TokenInfo x = token_info(p, i < p.T ? i : 0);
-        int32_t jn = i < p.T ? fetch(x, i, 0) : -1;
-        for (; i < p.T && ok; i += gridDim.x, ++tok) {
+        int32_t jn = i < p.T ? fetch(x, i, crank) : -1;
+        for (; i < p.T && ok; i += istep, ++tok) {
             if (lw == 0 && lane == 0) {
                 ok = mbar_wait(q_free, (tok & 1) ^ 1, abort_flag, p.status);
                 if (ok) {
@@ -290,9 +346,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 }
             }
             ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
-            const int inext = i + static_cast<int>(gridDim.x);
+            const int inext = i + istep;
             const TokenInfo xnext = token_info(p, inext < p.T ? inext : i);
-            for (int b = 0; b < x.nb && ok; ++b, ++g) {
+            for (int b = crank; b < x.nb && ok; b += kSplit, ++g) {
                 const int row = row_of(x, b, jn);
                 const uint8_t *src_base =
                     reinterpret_cast<const uint8_t *>(b < x.nwb ? p.raw_kv : p.pooled_kv) + pc * 16;
@@ -310,8 +366,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     cp_async16((par ? x_base : kv_base + 7 * 16384) + off, src + 7 * 128);
                 }
                 cp_async_arrive(&x_full[par]);
-                jn = (b + 1 < x.nb) ? fetch(x, i, b + 1)
-                                    : (inext < p.T ? fetch(xnext, inext, 0) : -1);
+                jn = (b + kSplit < x.nb) ? fetch(x, i, b + kSplit)
+                                         : (inext < p.T ? fetch(xnext, inext, crank) : -1);
                 // chunk pairs 0-2, then chunk 6, as the previous block's PV releases them
                 for (int m = 0; m < 4 && ok; ++m) {
                     if (lane == 0) ok = mbar_wait(&kv_free[m], (g & 1) ^ 1, abort_flag, p.status);
@@ -334,10 +390,18 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         // no copy into this CTA's shared memory may still be in flight at exit
         asm volatile("cp.async.wait_all;" ::: "memory");
         if (lw == 0 && lane == 0 && last_q >= 0) drain_wait(q_full, last_q & 1);
+        __syncwarp();
+        if constexpr (kSplit > 1) {
+            // the three cluster barriers of the softmax warps' merge
+            cluster_sync();
+            cluster_sync();
+            cluster_sync();
+        }
       } else if (warp == kQkWarp) {
         // ---------------- QK issuer (warp 6): S^T = K_blk . Q_t^T, chunk pair by chunk pair
         // as rows land. The whole warp runs the loop (descriptors stay warp-uniform) and
         // lane 0 issues: a lone diverged lane issues MMAs markedly slower.
+        DSA_SPLIT_COORDS
         const uint32_t leader = lane == 0;
         constexpr uint32_t idesc_qk = idesc_bf16(128, 64, false, false);
         const uint64_t ad0 = desc_sw128(smem_u32(sKV), 16, 1024);
@@ -345,11 +409,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const uint64_t bd0 = desc_sw128(smem_u32(sQ), 16, 1024);
         int tok = 0, g = 0;
         bool ok = true;
-        for (int i = blockIdx.x; i < p.T && ok; i += gridDim.x, ++tok) {
+        for (int i = i0; i < p.T && ok; i += istep, ++tok) {
             const TokenInfo x = token_info(p, i);
             if (!(ok = mbar_wait(q_full, tok & 1, abort_flag, p.status))) break;
             tc_fence_after();
-            for (int b = 0; b < x.nb && ok; ++b, ++g) {
+            for (int b = crank; b < x.nb && ok; b += kSplit, ++g) {
                 // S^T is double-buffered: the softmax of the block two back must have read
                 // this buffer; then QK can start while the previous block's softmax runs
                 const int par = g & 1;
@@ -389,32 +453,38 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 }
                 if (!ok) break;
                 mma_commit_if(s_full, leader);
-                if (b == x.nb - 1) mma_commit_if(q_free, leader);
+                if (last_block<kSplit>(b, x.nb)) mma_commit_if(q_free, leader);
             }
         }
         mma_commit_if(&drain[0], leader);
         if (leader) drain_wait(&drain[0], 0);
         __syncwarp();
+        if constexpr (kSplit > 1) {
+            cluster_sync();
+            cluster_sync();
+            cluster_sync();
+        }
       } else {
         // ---------------- PV issuer (warp 7): O^T += V_blk^T . P^T, one d-tile at a time;
         // whole warp in the loop, lane 0 issues the 32 MMAs of a block in one straight run
+        DSA_SPLIT_COORDS
         const uint32_t leader = lane == 0;
         constexpr uint32_t idesc_pv = idesc_bf16(128, 64, true, true);
         int tok = 0, g = 0;
         bool ok = true;
         if (leader) mbar_arrive(s_full);  // no PV precedes the first block
         __syncwarp();
-        for (int i = blockIdx.x; i < p.T && ok; i += gridDim.x, ++tok) {
+        for (int i = i0; i < p.T && ok; i += istep, ++tok) {
             const TokenInfo x = token_info(p, i);
-            for (int b = 0; b < x.nb && ok; ++b, ++g) {
+            for (int b = crank; b < x.nb && ok; b += kSplit, ++g) {
                 if (!(ok = mbar_wait(p_full, g & 1, abort_flag, p.status))) break;
                 tc_fence_after();
-                if (b == 0 && tok > 0) {
+                if (b == crank && tok > 0) {
                     // the epilogue of the previous token must have read O^T
                     if (!(ok = mbar_wait(o_free, (tok - 1) & 1, abort_flag, p.status))) break;
                     tc_fence_after();
                 }
-                const uint32_t acc0 = b > 0;
+                const uint32_t acc0 = b > crank;
                 // d-tile 3 is chunks 6 and 7: on odd blocks chunk 7 sits in the spare slot
                 const uint32_t lbo3 = (g & 1) ? kLbo7Spare : 16384u;
                 if (leader) {
@@ -432,17 +502,23 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 }
                 __syncwarp();
                 mma_commit_if(s_full, leader);
-                if (b == x.nb - 1) mma_commit_if(o_full, leader);
+                if (last_block<kSplit>(b, x.nb)) mma_commit_if(o_full, leader);
             }
         }
         mma_commit_if(&drain[1], leader);
         if (leader) drain_wait(&drain[1], 0);
         __syncwarp();
+        if constexpr (kSplit > 1) {
+            cluster_sync();
+            cluster_sync();
+            cluster_sync();
+        }
       }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegsSoft));
         // ---------------- softmax + epilogue, 8 warps: TMEM lanes of sub-partition sp
         // (keys, later dims) x heads [32*hh, 32*hh+32)
+        DSA_SPLIT_COORDS
         const int st = threadIdx.x - 32 * kSoftWarp0;
         const int sp = warp & 3;
         const int hh = (warp - kSoftWarp0) >> 2;
@@ -450,14 +526,14 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const int kl = sp * 32 + lane;
         const uint32_t lane_base = tmem + (static_cast<uint32_t>(sp * 32) << 16);
         int tok = 0, g = 0, cur = 0;
-        for (int i = blockIdx.x; i < p.T; i += gridDim.x, ++tok) {
+        for (int i = i0; i < p.T; i += istep, ++tok) {
             const TokenInfo x = token_info(p, i);
             float l[32];
 #pragma unroll
             for (int h = 0; h < 32; ++h) l[h] = 0.0f;
             if (sp == 0) sM[cur * 64 + hb + lane] = -INFINITY;
             bar_group(hh);
-            for (int b = 0; b < x.nb; ++b, ++g) {
+            for (int b = crank; b < x.nb; b += kSplit, ++g) {
                 bool valid;
                 if (b < x.nwb) {
                     valid = x.u0 + 128 * b + kl <= x.t;
@@ -530,7 +606,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         l[h] *= sAlpha[hb + h];
                         xv[h] = fmaf(__uint_as_float(sa[h]), p.c, -m_now[h]);
                     }
-                    if (b > 0 && live) {
+                    if (b > crank && live) {
 #pragma unroll 1
                         for (int m = 0; m < 4; ++m) {
                             uint32_t oa[32];
@@ -608,41 +684,156 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 l[0] = keep + __shfl_xor_sync(0xFFFFFFFFu, send, 1);
             }
             sL[sp * 64 + hb + lane] = l[0];
-            bar_soft();
-            if (st < 64) sLinv[st] = 1.0f / (sL[st] + sL[64 + st] + sL[128 + st] + sL[192 + st]);
-            bar_soft();
-            // O^T (4 d-tiles x this warp's 32 heads) into registers one tile at a time, scaled
-            // and stored straight to global memory: lane holds dim d = 128m + 32sp + lane of
-            // heads hb..hb+31, so for each head the warp writes 32 consecutive dims (64
-            // contiguous bytes). No staging in shared memory, so P's buffer stays free.
-            const bool live = mbar_wait(o_full, tok & 1, abort_flag, p.status);
-            tc_fence_after();
-            __nv_bfloat16 *orow = p.out + (static_cast<int64_t>(i) * kH + hb) * kD + 32 * sp + lane;
+            if constexpr (kSplit == 1) {
+                bar_soft();
+                if (st < 64) sLinv[st] = 1.0f / (sL[st] + sL[64 + st] + sL[128 + st] + sL[192 + st]);
+                bar_soft();
+                // O^T (4 d-tiles x this warp's 32 heads) into registers one tile at a time, scaled
+                // and stored straight to global memory: lane holds dim d = 128m + 32sp + lane of
+                // heads hb..hb+31, so for each head the warp writes 32 consecutive dims (64
+                // contiguous bytes). No staging in shared memory, so P's buffer stays free.
+                const bool live = mbar_wait(o_full, tok & 1, abort_flag, p.status);
+                tc_fence_after();
+                __nv_bfloat16 *orow = p.out + (static_cast<int64_t>(i) * kH + hb) * kD + 32 * sp + lane;
 #pragma unroll 1
-            for (int m = 0; m < 4; ++m) {
-                uint32_t oa[32];
-                if (live) {
+                for (int m = 0; m < 4; ++m) {
+                    uint32_t oa[32];
+                    if (live) {
+                        tmem_ld32(lane_base + kOCol + 64 * m + hb, oa);
+                        tmem_wait_ld();
+                    }
+                    if (live) {
+                        __nv_bfloat16 *o = orow + 128 * m;
+#pragma unroll
+                        for (int h = 0; h < 32; ++h)
+                            o[h * kD] = __float2bfloat16_rn(__uint_as_float(oa[h]) * sLinv[hb + h]);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(o_free);
+            } else {
+                // ---- merge of the cluster's partial results: CTA r holds, per head,
+                // its running max m_r, sum l_r and O_r^T over its own blocks. With
+                // M = max_r m_r and L = sum_r l_r 2^(m_r - M), the output is
+                // sum_r O_r 2^(m_r - M) / L.
+                const bool has = crank < x.nb;
+                const bool live = has && mbar_wait(o_full, tok & 1, abort_flag, p.status);
+                tc_fence_after();
+                bar_soft();
+                // P's buffer is free once the last PV is done: it carries (m_r, l_r)
+                float *sXm = reinterpret_cast<float *>(sP);
+                float *sXl = sXm + 64;
+                if (st < 64) {
+                    sXm[st] = has ? sM[cur * 64 + st] : -INFINITY;
+                    sXl[st] = sL[st] + sL[64 + st] + sL[128 + st] + sL[192 + st];
+                }
+                cluster_sync();
+                if (st < 64) {
+                    float mr[kSplit], lr[kSplit];
+                    float mx = -INFINITY;
+#pragma unroll
+                    for (int r = 0; r < kSplit; ++r) {
+                        mr[r] = ld_peer(peer_addr(smem_u32(&sXm[st]), r));
+                        lr[r] = ld_peer(peer_addr(smem_u32(&sXl[st]), r));
+                        mx = fmaxf(mx, mr[r]);
+                    }
+                    float tot = 0.0f;
+#pragma unroll
+                    for (int r = 0; r < kSplit; ++r)
+                        if (lr[r] > 0.0f) tot += lr[r] * ex2(mr[r] - mx);
+                    sLinv[st] = sXl[st] > 0.0f ? ex2(sXm[st] - mx) / tot : 0.0f;
+                }
+                bar_soft();
+                // this CTA's scaled O^T, fp32 [64 heads][512 dims], into its key tile
+                // (free: the token's last PV is done and no token follows)
+                float *stage = reinterpret_cast<float *>(sKV);
+#pragma unroll 1
+                for (int m = 0; m < 4; ++m) {
+                    // (loaded even when this CTA ran no PV: a read of allocated but
+                    // unwritten TMEM columns is harmless, and the value is dropped below)
+                    uint32_t oa[32];
                     tmem_ld32(lane_base + kOCol + 64 * m + hb, oa);
                     tmem_wait_ld();
-                }
-                if (live) {
-                    __nv_bfloat16 *o = orow + 128 * m;
+                    float *col = stage + hb * kD + 128 * m + 32 * sp + lane;
 #pragma unroll
                     for (int h = 0; h < 32; ++h)
-                        o[h * kD] = __float2bfloat16_rn(__uint_as_float(oa[h]) * sLinv[hb + h]);
+                        col[h * kD] = live ? __uint_as_float(oa[h]) * sLinv[hb + h] : 0.0f;
                 }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(o_free);
+                cluster_sync();
+                // dims [64 crank, 64 crank + 64) of every head: the sum over the cluster's
+                // CTAs in rank order, rounded to bf16
+                const uint32_t stage_u = smem_u32(stage);
+#pragma unroll 1
+                for (int it = st; it < kH * 16; it += kSoftThreads) {
+                    const int h = it >> 4, q4 = it & 15;
+                    const uint32_t off = static_cast<uint32_t>(h * kD + 64 * crank + 4 * q4) * 4u;
+                    float4 acc = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+#pragma unroll
+                    for (int r = 0; r < kSplit; ++r) {
+                        const float4 v = ld_peer4(peer_addr(stage_u + off, r));
+                        acc.x += v.x;
+                        acc.y += v.y;
+                        acc.z += v.z;
+                        acc.w += v.w;
+                    }
+                    const __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
+                    const __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+                    uint2 pk;
+                    pk.x = *reinterpret_cast<const uint32_t *>(&lo);
+                    pk.y = *reinterpret_cast<const uint32_t *>(&hi);
+                    *reinterpret_cast<uint2 *>(p.out + (static_cast<int64_t>(i) * kH + h) * kD +
+                                               64 * crank + 4 * q4) = pk;
+                }
+                // no CTA leaves (or reuses its shared memory) while the others read it
+                cluster_sync();
             }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(o_free);
         }
     }
+#undef DSA_SPLIT_COORDS
     __syncthreads();
     if (warp == kPvWarp) {
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, 512);
     }
+}
+
+// CTAs per token in the split mode (a portable cluster size).
+constexpr int kSplitN = 8;
+
+template <int kSplit>
+int prepare_attention() {
+    // the setmaxnreg split is only safe with the launch allocation it assumes
+    cudaFuncAttributes fa;
+    if (cudaFuncGetAttributes(&fa, attn_kernel<kSplit>) != cudaSuccess ||
+        fa.numRegs != kRegsLaunch)
+        return DSA_ERR_CUDA;
+    if (cudaFuncSetAttribute(attn_kernel<kSplit>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             kAttnSmem) != cudaSuccess)
+        return DSA_ERR_CUDA;
+    return DSA_OK;
+}
+
+cudaLaunchConfig_t split_config(unsigned grid, cudaStream_t s) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid, 1, 1);
+    cfg.blockDim = dim3(kAttnThreads, 1, 1);
+    cfg.dynamicSmemBytes = kAttnSmem;
+    cfg.stream = s;
+    return cfg;
+}
+
+cudaLaunchAttribute cluster_attr() {
+    cudaLaunchAttribute at = {};
+    at.id = cudaLaunchAttributeClusterDimension;
+    at.val.clusterDim.x = kSplitN;
+    at.val.clusterDim.y = 1;
+    at.val.clusterDim.z = 1;
+    return at;
 }
 
 }  // namespace
@@ -653,14 +844,19 @@ int launch_attention(const void *q, const void *raw_kv, int64_t raw_start, int64
                      void *out, int32_t *status, cudaStream_t s) {
     (void)raw_rows;
     static bool checked = false;
+    static bool split_ok = false;
     if (!checked) {
-        // the setmaxnreg split is only safe with the launch allocation it assumes
-        cudaFuncAttributes fa;
-        if (cudaFuncGetAttributes(&fa, attn_kernel) != cudaSuccess || fa.numRegs != kRegsLaunch)
+        if (prepare_attention<1>() != DSA_OK || prepare_attention<kSplitN>() != DSA_OK)
             return DSA_ERR_CUDA;
-        if (cudaFuncSetAttribute(attn_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kAttnSmem) != cudaSuccess)
-            return DSA_ERR_CUDA;
+        // can a cluster of kSplitN whole-SM CTAs be resident at all?
+        int nc = 0;
+        cudaLaunchConfig_t cfg = split_config(kSplitN, nullptr);
+        cudaLaunchAttribute at = cluster_attr();
+        cfg.attrs = &at;
+        cfg.numAttrs = 1;
+        split_ok = cudaOccupancyMaxActiveClusters(&nc, attn_kernel<kSplitN>, &cfg) == cudaSuccess &&
+                   nc > 0;
+        (void)cudaGetLastError();
         checked = true;
     }
     CUtensorMap tm_q;
@@ -680,8 +876,24 @@ int launch_attention(const void *q, const void *raw_kv, int64_t raw_start, int64
     p.c = scale * 1.4426950408889634f;
     p.T = static_cast<int>(chunk);
     p.status = status;
-    const int grid = static_cast<int>(std::min<int64_t>(chunk, std::max(1, sm_count())));
-    attn_kernel<<<grid, kAttnThreads, kAttnSmem, s>>>(tm_q, p);
+    const int sms = std::max(1, sm_count());
+    // key blocks of the chunk's last token (the most of any of its tokens)
+    const int64_t t_last = offset + chunk - 1;
+    const int64_t nv = std::min(n, (t_last + 1) / ratio);
+    const int64_t nwin = t_last - std::max<int64_t>(0, t_last - window + 1) + 1;
+    const int64_t nb = (nwin + 127) / 128 + (std::min<int64_t>(k, nv) + 127) / 128;
+    if (split_ok && chunk * kSplitN <= sms && nb > 1) {
+        // few tokens: a cluster per token spreads its key blocks over kSplitN SMs
+        cudaLaunchConfig_t cfg = split_config(static_cast<unsigned>(chunk * kSplitN), s);
+        cudaLaunchAttribute at = cluster_attr();
+        cfg.attrs = &at;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, attn_kernel<kSplitN>, tm_q, p) != cudaSuccess)
+            return DSA_ERR_CUDA;
+        return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
+    }
+    const int grid = static_cast<int>(std::min<int64_t>(chunk, sms));
+    attn_kernel<1><<<grid, kAttnThreads, kAttnSmem, s>>>(tm_q, p);
     return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
