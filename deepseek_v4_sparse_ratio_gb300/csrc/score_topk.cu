@@ -498,10 +498,11 @@ __global__ void __launch_bounds__(NT)
     // ---- 1. range of the row
     float vmin = INFINITY, vmax = -INFINITY;
     if (nseg > 0) {
-        if (warp == 0 && lane < nseg) {
-            vmin = __int_as_float(out[2 * lane]);
-            vmax = __int_as_float(out[2 * lane + 1]);
-        }
+        if (warp == 0)
+            for (int sg = lane; sg < nseg; sg += 32) {
+                vmin = fminf(vmin, __int_as_float(out[2 * sg]));
+                vmax = fmaxf(vmax, __int_as_float(out[2 * sg + 1]));
+            }
     } else {
         for (int64_t j = lo + lane; j < hi; j += 32) {
             const float v = src[j];
@@ -658,7 +659,9 @@ __global__ void fill_selection_kernel(int32_t *sel, int64_t rows, int32_t k, int
 int choose_segments(int groups, int NB, int sms) {
     int best = 1;
     double best_cost = 1e30;
-    for (int ns = 1; ns <= std::min(32, NB); ++ns) {
+    // (up to 32 segments; more when the row groups alone leave SMs idle)
+    const int cap = std::min(NB, std::max(32, sms / std::max(1, groups)));
+    for (int ns = 1; ns <= cap; ++ns) {
         const int64_t units = static_cast<int64_t>(groups) * ns;
         const int64_t waves = (units + sms - 1) / sms;
         const double cost = static_cast<double>(waves) * (static_cast<double>(NB) / ns + 4.0);
