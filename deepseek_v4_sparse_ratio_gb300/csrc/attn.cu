@@ -33,6 +33,14 @@
 // on most blocks without changing the result (the same max divides out at the
 // end). Output = O^T / sum, bf16, stored by the softmax warps straight from the
 // registers they read O^T into.
+//
+// Few tokens (decode steps, short bands): one CTA per token would leave most SMs
+// idle while it walks the token's blocks in sequence, so a cluster of 8 CTAs
+// takes each token instead. CTA r takes blocks r, r+8, ... with its own online
+// softmax; at the token's end the CTAs exchange (running max, sum) per head
+// through distributed shared memory, scale their O^T by 2^(m_r - M) / L, stage
+// it in their (now free) key tiles, and each sums one 64-dim slice of every head
+// over the cluster. No global scratch is involved.
 #include <math.h>
 
 #include <algorithm>

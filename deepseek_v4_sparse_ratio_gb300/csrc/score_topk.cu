@@ -15,8 +15,9 @@
 // Score kernel (tcgen05): s[t,j] = sum_h w[t,h] * ReLU(q[t,h,:] . k[j,:]).
 // The contraction is a GEMM with the pooled keys on M (128 rows per MMA) and
 // (token, head) pairs on N (4 tokens x 64 heads = 256), K = 128. A persistent
-// CTA keeps the indexer queries of 8 tokens resident in shared memory (two
-// N=256 operands) and streams 128-row key blocks through a TMA ring; the
+// CTA works through units of (8 tokens, one segment of the key range): it keeps
+// the indexer queries of the 8 tokens resident in shared memory (two N=256
+// operands) and streams the segment's 128-row key blocks through a TMA ring; the
 // accumulators live in TMEM (2 x 256 columns, one per 4-token half), so the
 // epilogue thread that owns TMEM lane j holds every head of its tokens for
 // pooled row j and reduces them in registers: ReLU, multiply by w, sum over
