@@ -372,7 +372,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 // ------------------------------------------------------------------ top-k kernel
 
 // threads per top-k CTA: 256 (several CTAs per SM) when the tile has rows
-// enough to fill the GPU, else 1024, so a few rows walk their scores 4x faster
+// enough to fill the GPU and the rows are short, else 1024
 constexpr int kTopkThreads = 256;
 constexpr int kTopkThreadsFew = 1024;
 constexpr int kBins = 2048;
@@ -724,7 +724,10 @@ int launch_topk_tile(const float *scores, int64_t stride, int64_t n, int64_t off
                      int32_t ratio, int64_t r0, int64_t R, int32_t k, int32_t nseg_rng,
                      int32_t *sel, int32_t *status, cudaStream_t s) {
     (void)status;
-    if (R < 2 * static_cast<int64_t>(sm_count()))
+    // 1024-thread CTAs (one per SM) for tiles of few rows, and for long rows: with
+    // rows over 64K scores (256 KB) four CTAs per SM would keep more rows in flight
+    // than L2 holds, and every pass after the first would go back to HBM
+    if (R < 2 * static_cast<int64_t>(sm_count()) || n > 65536)
         topk_kernel<kTopkThreadsFew><<<static_cast<unsigned>(R), kTopkThreadsFew, 0, s>>>(
             scores, stride, n, offset, ratio, r0, k, nseg_rng, sel);
     else
