@@ -77,12 +77,12 @@ def work_counts(wl):
 NCU_TRAFFIC = {
     "attn_kernel": {"bytes": 343.8e6 + 234.5e6, "files": ("attn.cu", "common.cuh", "internal.h"),
                     "sha256_16": "991b2ad1da88f9f9"},
-    "score_kernel": {"bytes": 77.1e6 + 477.7e6,
+    "score_kernel": {"bytes": 77.7e6 + 477.5e6,
                      "files": ("score_topk.cu", "common.cuh", "internal.h"),
-                     "sha256_16": "e0a5cf2592e841d4"},
-    "topk_kernel": {"bytes": 563.0e6 + 31.3e6,
+                     "sha256_16": "b84f7a0fd5fe9733"},
+    "topk_kernel": {"bytes": 563.6e6 + 31.0e6,
                     "files": ("score_topk.cu", "common.cuh", "internal.h"),
-                    "sha256_16": "e0a5cf2592e841d4"},
+                    "sha256_16": "b84f7a0fd5fe9733"},
 }
 
 
