@@ -104,6 +104,54 @@ def test_pool_is_rounded_exact_mean():
     assert np.array_equal(got, _nearest_bf16_bruteforce(mean))
 
 
+@pytest.mark.parametrize("ratio", [2, 8, 32, 128])
+def test_pool_any_ratio_is_rounded_exact_rational_mean(ratio):
+    """Every power-of-two ratio: the exact mean (rational arithmetic, no floating
+    sum at all), rounded once to the nearest bf16. Columns 0 and 1 start each group
+    with 2^10, 2^-20, -2^10, which a running fp32 sum would round; column 0 then
+    holds zeros, so its exact mean is 2^-20 / ratio, column 1 random values."""
+    from fractions import Fraction
+    x = torch.randn(2 * ratio, 24, generator=torch.Generator().manual_seed(ratio))
+    for c in (0, 1):
+        x[0::ratio, c], x[1::ratio, c], x[2::ratio, c] = 2.0 ** 10, 2.0 ** -20, -(2.0 ** 10)
+    for r in range(3, ratio):
+        x[r::ratio, 0] = 0.0
+    xs = oracle.bf16_bits_to_f64(oracle.as_bf16_bits(x.to(torch.bfloat16)))
+    got = oracle.pool_rows(x.to(torch.bfloat16), ratio)
+    mean = np.empty((2, 24))
+    for g in range(2):
+        for c in range(24):
+            m = sum(Fraction(v) for v in xs[g * ratio:(g + 1) * ratio, c]) / ratio
+            assert Fraction(float(m)) == m   # representable in fp64: no rounding yet
+            mean[g, c] = float(m)
+    assert np.array_equal(got, _nearest_bf16_bruteforce(mean))
+    if ratio == 2:   # group [2^10, 2^-20]: mean 2^9 + 2^-21 rounds to 2^9
+        assert got[0, 0] == _nearest_bf16_bruteforce(np.array([2.0 ** 9]))[0]
+    else:            # [2^10, 2^-20, -2^10, 0, ...]: the mean is exactly 2^-20 / ratio
+        assert got[0, 0] == _nearest_bf16_bruteforce(np.array([2.0 ** -20 / ratio]))[0]
+
+
+@pytest.mark.parametrize("ratio", [16, 128])
+def test_pool_closed_forms_large_ratio(ratio):
+    """n = floor(N/ratio) and rem = N mod ratio after every chunk; chunking changes
+    no pooled row."""
+    rng = np.random.default_rng(ratio)
+    N = 3 * ratio + ratio // 2 + 1
+    ik, kv = _bf16((N, 128), 41), _bf16((N, 512), 42)
+    one = oracle.PoolState(ratio)
+    one.append(ik, kv, 0)
+    for trial in range(6):
+        cuts = sorted(rng.choice(np.arange(1, N), size=rng.integers(1, 6), replace=False))
+        st = oracle.PoolState(ratio)
+        prev = 0
+        for c in list(cuts) + [N]:
+            st.append(ik[prev:c], kv[prev:c], prev)
+            assert st.n_pooled == c // ratio and st.n_rem == c % ratio
+            prev = c
+        assert np.array_equal(st.pooled_ik, one.pooled_ik)
+        assert np.array_equal(st.pooled_kv, one.pooled_kv)
+
+
 def test_pool_closed_forms_and_chunking_invariance():
     rng = np.random.default_rng(5)
     N = 37
