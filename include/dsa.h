@@ -186,6 +186,12 @@ int dsa_index_score_topk(const void *q_idx, const float *w, const void *pooled_i
  *   entries are read; among them -1 is skipped, and an index outside
  *   [0, n_vis(t)) is skipped and reported as DSA_ERR_BOUNDS in dev_status;
  *   window > 0; scale > 0; out [chunk, 64, 512] bf16.
+ * Launch shape: one 512-thread CTA per SM, each taking whole tokens; for a
+ * chunk of at most (SM count / 8) rows whose tokens span more than one
+ * 128-key block (decode steps, short bands), thread-block clusters of 8 CTAs
+ * per token instead, merging their partial softmax results through
+ * distributed shared memory (no memory beyond the arguments is used). The
+ * result differs between the two shapes only by floating-point rounding.
  * Errors: DSA_ERR_ARG, DSA_ERR_SHAPE, DSA_ERR_RAW_RANGE, DSA_ERR_CUDA.
  */
 int dsa_window_sparse_attn(const void *q, const void *raw_kv, int64_t raw_start,
