@@ -1,4 +1,6 @@
-// Step (a): ratio-4 mean pooling of a chunk's raw rows into the PoolingCache.
+// Step (a): mean pooling of a chunk's raw rows into the PoolingCache (ratio 4
+// for the indexed attention; any power of two up to 128, e.g. the compressed
+// attention's 128).
 //
 // "perf(deepseek-v4): skip redundant all-pooled indexer scoring", Summary and
 // Correctness: the attention-KV and indexer-key compressors both run once per
