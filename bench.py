@@ -216,7 +216,7 @@ def cpu_baseline(wl, seconds_budget: float = 20.0, max_rows: int = 4096):
     # pooling is per chunk: charge its share per row
     per_row = elapsed / rows_done + t_pool / T
     return {"value": 1.0 / per_row, "unit": UNIT, "cores": oracle.threads(), "kind": "oracle",
-            "sample": f"{rows_done} evenly spaced query rows of the 4096-row chunk "
+            "sample": f"{rows_done} evenly spaced query rows of the {T}-row chunk "
                       f"(score all visible pooled rows + top-k + attention, fp64), "
                       f"plus the chunk's pooling", "seconds": elapsed + t_pool}
 
