@@ -5,9 +5,11 @@ method's arithmetic (no pooling, scoring, selection or attention), so both the
 CPU oracle and the CUDA path can take their inputs from it.
 
 Shapes and distributions follow the workloads the pages discuss for
-DeepSeek-V4 chunked prefill (omlx PR #2563 "Performance evidence": 2,048-token
-prefill steps; ds4 issue #644 "128 GB / 1M-context motivation": a 4,096-token
-global chunk at 1,048,576 tokens of context): B=1, indexer heads H_I=64 of dim
+DeepSeek-V4 chunked prefill ("perf(deepseek-v4): skip redundant all-pooled
+indexer scoring", Performance evidence: 2,048-token prefill steps; "[Discussion]
+Tile indexed-attention scoring independently of the global prefill chunk",
+128 GB / 1M-context motivation: a 4,096-token global chunk at 1,048,576 tokens
+of context): B=1, indexer heads H_I=64 of dim
 d_I=128, attention heads H=64 over one shared KV row of dim D=512, all values
 drawn ~N(0,1) in fp32 and rounded to bf16, indexer head weights ~N(0,1/64) kept
 in fp32.
