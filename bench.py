@@ -105,8 +105,10 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv") \
-            if os.path.isdir(os.path.join(ROOT, "gpurun_out")) else f"/tmp/dsa_clocks_{os.getpid()}.csv"
+        # the raw samples go to $DSA_CLOCKS_DIR when set (kept for inspection), else /tmp
+        d = os.environ.get("DSA_CLOCKS_DIR")
+        self.path = (os.path.join(d, f"clocks_rank{index}.csv") if d and os.path.isdir(d)
+                     else f"/tmp/dsa_clocks_{os.getpid()}_{index}.csv")
 
     def __enter__(self):
         q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
