@@ -181,6 +181,17 @@ def max_over_ranks(x, world, device):
     return float(t.item())
 
 
+def step_launches(wl, tile):
+    """Kernels one dsa_prefill_chunk step launches on the workload's chunk: pooling
+    when a pooled row completes, the remainder copy when tokens are left over, the
+    selection fill (skip path) or score + top-k per tile, and the attention."""
+    T, off, r = wl.chunks[0], wl.off0, wl.ratio
+    n_old, n = off // r, (off + T) // r
+    pool = (1 if n > n_old else 0) + (1 if (off + T) % r else 0)
+    select = 1 if n <= wl.index_topk else 2 * math.ceil(T / tile)
+    return pool + select + 1
+
+
 def job_throughput(units_per_rank, world, ms):
     """Whole-job rate: the units all ranks processed / the slowest rank's step time."""
     return world * units_per_rank / (ms * 1e-3)
@@ -430,10 +441,7 @@ def main():
     st_tf = counts["score_flops"] / (comp_ms["score_topk"] * 1e-3) / 1e12
     attn_traffic = ncu_traffic("attn_kernel", args.workload)
     skip = n <= wl.index_topk
-    n_tiles = 0 if skip else math.ceil(T / tile)
-    launches_per_step = (1 + (1 if (wl.off0 + T) % r else 0)   # pool (+ remainder)
-                         + (1 if skip else 2 * n_tiles)          # fill, or score+top-k per tile
-                         + 1)                                    # attention
+    launches_per_step = step_launches(wl, tile)
     if skip:
         # nothing is scored on the skip path: a selection fill only
         st_roof = {"kernel": "fill_selection_kernel (dsa_index_score_topk skip path: every "

@@ -56,3 +56,13 @@ def test_both_bench_arms_print_the_same_config():
     a = bench.run_config(wl, "ctx_128k", 4096, 1)
     b = bench.run_config(wl, bench.WORKLOAD, 4096, 1)
     assert a == b and a["pooled_rows"] == 32768 and a["chunk"] == 4096
+
+
+def test_launch_counts_match_the_launch_lists():
+    """4 kernels a step at 128K (pool, score, top-k, attention: profiles'
+    launch list); 4 for the decode step (remainder copy instead of pooling);
+    2 per extra indexer tile; 3 on the skip path (pool, fill, attention)."""
+    assert bench.step_launches(inputs.workload("ctx_128k"), 4096) == 4
+    assert bench.step_launches(inputs.workload("decode_128k"), 1) == 4
+    assert bench.step_launches(inputs.workload("ctx_1m"), 1024) == 1 + 8 + 1
+    assert bench.step_launches(inputs.workload("compressed_128k"), 4096) == 3
