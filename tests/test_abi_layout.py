@@ -1,0 +1,48 @@
+"""The ctypes structures of the Python binding have the layout of the C ABI's
+structures: a small C program compiled against include/dsa.h prints every
+field's offset and each structure's size, and the binding must agree (a
+mismatch would hand the library shifted fields). Needs only gcc."""
+import ctypes
+import os
+import shutil
+import subprocess
+import tempfile
+
+import pytest
+
+from deepseek_v4_sparse_ratio_gb300 import _binding as B
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+STRUCTS = {"dsa_pool_state": B.dsa_pool_state, "dsa_prefill_workspace": B.dsa_prefill_workspace}
+
+
+def _c_layout():
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    lines = ["#include <stddef.h>", "#include <stdio.h>", '#include "dsa.h"', "int main(void) {"]
+    for name, cls in STRUCTS.items():
+        lines.append(f'  printf("{name} size %zu\\n", sizeof({name}));')
+        for field, _ in cls._fields_:
+            lines.append(f'  printf("{name} {field} %zu\\n", offsetof({name}, {field}));')
+    lines += ["  return 0;", "}"]
+    with tempfile.TemporaryDirectory() as d:
+        src, exe = os.path.join(d, "layout.c"), os.path.join(d, "layout")
+        with open(src, "w") as fh:
+            fh.write("\n".join(lines) + "\n")
+        subprocess.run([cc, "-std=c11", "-I", os.path.join(ROOT, "include"), src, "-o", exe],
+                       check=True, capture_output=True)
+        out = subprocess.run([exe], check=True, capture_output=True, text=True).stdout
+    layout = {}
+    for line in out.splitlines():
+        name, field, value = line.split()
+        layout[(name, field)] = int(value)
+    return layout
+
+
+def test_binding_structs_match_the_c_header():
+    layout = _c_layout()
+    for name, cls in STRUCTS.items():
+        assert ctypes.sizeof(cls) == layout[(name, "size")], name
+        for field, _ in cls._fields_:
+            assert getattr(cls, field).offset == layout[(name, field)], (name, field)
