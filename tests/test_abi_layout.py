@@ -46,3 +46,37 @@ def test_binding_structs_match_the_c_header():
         assert ctypes.sizeof(cls) == layout[(name, "size")], name
         for field, _ in cls._fields_:
             assert getattr(cls, field).offset == layout[(name, field)], (name, field)
+
+
+def _prototypes():
+    """name -> parameter count, from the prototypes in include/dsa.h."""
+    import re
+    text = open(os.path.join(ROOT, "include", "dsa.h")).read()
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    protos = {}
+    for m in re.finditer(r"\b(?:int|size_t|const char \*)\s*(dsa_\w+)\s*\(([^;{]*?)\)\s*;", text):
+        params = [p for p in m.group(2).split(",") if p.strip() and p.strip() != "void"]
+        protos[m.group(1)] = len(params)
+    return protos
+
+
+def test_binding_argtypes_match_the_prototypes():
+    protos = _prototypes()
+    lib = B.load()
+    for name in B.EXPORTS:
+        assert name in protos, name
+        argtypes = getattr(lib, name).argtypes
+        if argtypes is not None:
+            assert len(argtypes) == protos[name], (name, len(argtypes), protos[name])
+
+
+def test_binding_error_codes_match_the_header():
+    import re
+    text = open(os.path.join(ROOT, "include", "dsa.h")).read()
+    codes = {m.group(1): int(m.group(2)) for m in re.finditer(r"\b(DSA_\w+)\s*=\s*(-?\d+)", text)}
+    errs = {k: v for k, v in codes.items() if k.startswith("DSA_ERR_") or k == "DSA_OK"}
+    assert len(errs) >= 11
+    for name, value in errs.items():
+        if hasattr(B, name):
+            assert getattr(B, name) == value, name
+    assert all(hasattr(B, n) for n in errs if n != "DSA_OK"), "an error code is missing"
