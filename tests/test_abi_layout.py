@@ -80,3 +80,11 @@ def test_binding_error_codes_match_the_header():
         if hasattr(B, name):
             assert getattr(B, name) == value, name
     assert all(hasattr(B, n) for n in errs if n != "DSA_OK"), "an error code is missing"
+
+
+def test_static_scratch_size_matches_the_header():
+    import re
+    text = open(os.path.join(ROOT, "include", "dsa.h")).read()
+    m = re.search(r"#define\s+DSA_STATIC_SCRATCH_BYTES\s+\(\(size_t\)(\d+)\s*<<\s*(\d+)\)", text)
+    assert m is not None
+    assert B.DSA_STATIC_SCRATCH_BYTES == int(m.group(1)) << int(m.group(2))
