@@ -6,8 +6,11 @@ A step is one call of dsa_prefill_chunk on the 128K-context workload: one
 synthetic pooled rows already cached), index_topk 2048, H_I=64/d_I=128,
 H=64/D=512 bf16, window 128 -- pool/append, indexer score + top-k (full path)
 and window + selected attention. Between steps the PoolingCache counters are
-rolled back (O(1)) and L2 is flushed with a 512 MiB write outside the timed
-events. Prints one JSON line (rank 0).
+rolled back (O(1)) and L2 is flushed with a 512 MiB write, both outside the
+timed events. Prints one JSON line (rank 0); its `configs` object times the
+other workloads the same way (a multi-chunk prompt's step is the whole prompt,
+chunk after chunk), with their attention and score + top-k fractions, clocks
+and peak score-scratch bytes.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 
@@ -53,22 +56,39 @@ def load_peaks():
 
 
 def work_counts(wl):
-    """Algorithmic work of one step: score flops, attention flops, bytes."""
-    T, off, k, W, r = wl.chunks[0], wl.off0, wl.index_topk, wl.window, wl.ratio
-    n = (off + T) // r
-    score_flops = attn_flops = 0
-    topk_bytes = 0
-    for i in range(T):
-        t = off + i
-        nv = min((t + 1) // r, n)
-        score_flops += 2 * 64 * 128 * nv
-        topk_bytes += 4 * nv
-        attn_flops += 4 * 64 * 512 * (min(W, t + 1) + min(k, nv))
+    """Algorithmic work of one step (every chunk of the workload once): score flops
+    (full-path chunks only: the skip path scores nothing), attention flops, bytes."""
+    k, W, r = wl.index_topk, wl.window, wl.ratio
+    score_flops = attn_flops = topk_bytes = score_read = score_write = pool_bytes = 0
+    for _, _, T, off in wl.chunk_bounds():
+        n = (off + T) // r
+        full = n > k
+        pool_bytes += T * 640 * 2 + ((off + T) // r - off // r) * 640 * 2
+        for i in range(T):
+            t = off + i
+            nv = min((t + 1) // r, n)
+            if full:
+                score_flops += 2 * 64 * 128 * nv
+                topk_bytes += 4 * nv
+            attn_flops += 4 * 64 * 512 * (min(W, t + 1) + min(k, nv))
+        if full:
+            topk_bytes += T * k * 4
+            score_read += T * 64 * 128 * 2 + T * 64 * 4 + n * 128 * 2
+            score_write += 4 * T * ((n + 127) // 128 * 128)
     return {"score_flops": score_flops, "attn_flops": attn_flops,
-            "score_read_bytes": T * 64 * 128 * 2 + T * 64 * 4 + n * 128 * 2,
-            "score_write_bytes": 4 * T * ((n + 127) // 128 * 128),
-            "topk_bytes": topk_bytes + T * k * 4,
-            "pool_bytes": T * 640 * 2 + (T // r) * 640 * 2}
+            "score_read_bytes": score_read, "score_write_bytes": score_write,
+            "topk_bytes": topk_bytes, "pool_bytes": pool_bytes}
+
+
+def score_scratch_bytes(wl, tile):
+    """Peak score-scratch bytes of the workload: one tile of the largest full-path chunk."""
+    from deepseek_v4_sparse_ratio_gb300 import _binding as B
+    peak = 0
+    for _, _, T, off in wl.chunk_bounds():
+        n = (off + T) // wl.ratio
+        if n > wl.index_topk:
+            peak = max(peak, B.dsa_score_scratch_bytes(min(tile, T), n))
+    return peak
 
 
 # DRAM bytes (read + write) per launch from one ncu capture of each kernel on the
@@ -182,14 +202,18 @@ def max_over_ranks(x, world, device):
 
 
 def step_launches(wl, tile):
-    """Kernels one dsa_prefill_chunk step launches on the workload's chunk: pooling
-    when a pooled row completes, the remainder copy when tokens are left over, the
-    selection fill (skip path) or score + top-k per tile, and the attention."""
-    T, off, r = wl.chunks[0], wl.off0, wl.ratio
-    n_old, n = off // r, (off + T) // r
-    pool = (1 if n > n_old else 0) + (1 if (off + T) % r else 0)
-    select = 1 if n <= wl.index_topk else 2 * math.ceil(T / tile)
-    return pool + select + 1
+    """Kernels one step launches (every chunk of the workload through
+    dsa_prefill_chunk): per chunk, pooling when a pooled row completes, the
+    remainder copy when tokens are left over, the selection fill (skip path) or
+    score + top-k per tile, and the attention."""
+    total = 0
+    r = wl.ratio
+    for _, _, T, off in wl.chunk_bounds():
+        n_old, n = off // r, (off + T) // r
+        pool = (1 if n > n_old else 0) + (1 if (off + T) % r else 0)
+        select = 1 if n <= wl.index_topk else 2 * math.ceil(T / tile)
+        total += pool + select + 1
+    return total
 
 
 def job_throughput(units_per_rank, world, ms):
@@ -297,6 +321,115 @@ def run_config(wl, name, tile, world):
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
 
 
+# The other workloads reported in the `configs` object of the JSON line: the
+# short zero-prefix prompt, the two-chunk 4,098-token prompt, the 16K prompt in
+# eight 2048-token chunks (a step = the whole prompt, chunk after chunk) and the
+# 1M-context chunk with 1024-row indexer tiles (1 GiB of score scratch).
+EXTRA_CONFIGS = (("zero_prefix_512", 0), ("two_chunks_4098", 0), ("prompt_16k", 0),
+                 ("ctx_1m", 1024))
+
+
+def component_times(dw, wl, tile, snap, flush, stream, reps):
+    """Per-step time of each ABI entry point called alone (pool, score + top-k,
+    attention), summed over the workload's chunks; mean over reps."""
+    import torch
+    from deepseek_v4_sparse_ratio_gb300 import _binding as B
+    comp = {"pool": [], "score_topk": [], "attention": []}
+    k, r = wl.index_topk, wl.ratio
+    for i in range(reps + 1):
+        flush.zero_()
+        dw.state.restore(snap)
+        e = []
+        for _, s, T, off in wl.chunk_bounds():
+            n = (off + T) // r
+            ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+            ev[0].record(stream)
+            B.dsa_pool_append(dw.state, dw.raw_kv[off - dw.raw_start:], dw.raw_ik[s:s + T], T, off,
+                              r, stream)
+            ev[1].record(stream)
+            B.dsa_index_score_topk(dw.q_idx[s:s + T], dw.w[s:s + T], dw.state.pooled_ik, n, T, off,
+                                   r, k, tile, dw.scratch, dw.sel[:T], dw.status, stream)
+            ev[2].record(stream)
+            B.dsa_window_sparse_attn(dw.q[s:s + T], dw.raw_kv, dw.raw_start, dw.state.pooled_kv,
+                                     n, dw.sel[:T], k, T, off, r, wl.window, dw.scale,
+                                     dw.out[:T], dw.status, stream)
+            ev[3].record(stream)
+            e.append(ev)
+        torch.cuda.synchronize()
+        if i >= 1:   # the first pass warms up
+            comp["pool"].append(sum(a[0].elapsed_time(a[1]) for a in e))
+            comp["score_topk"].append(sum(a[1].elapsed_time(a[2]) for a in e))
+            comp["attention"].append(sum(a[2].elapsed_time(a[3]) for a in e))
+    dw.check_status()
+    return {key: statistics.mean(v) for key, v in comp.items()}
+
+
+def time_steps(dw, wl, snap, flush, stream, steps, warmup, clock_index):
+    """W untimed steps, then K steps each bracketed by CUDA events on the launching
+    stream (a step = every chunk of the workload through dsa_prefill_chunk); the
+    state rollback and the L2 flush happen between the events, outside the step."""
+    import torch
+    nch = len(wl.chunks)
+    for _ in range(warmup):
+        flush.zero_()
+        dw.state.restore(snap)
+        for c in range(nch):
+            dw.run_chunk(c, stream)
+    torch.cuda.synchronize()
+    dw.check_status()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(steps)]
+    torch.cuda.synchronize()
+    with ClockSampler(clock_index) as clk:
+        w0 = time.perf_counter()
+        for i in range(steps):
+            flush.zero_()
+            dw.state.restore(snap)
+            ev[i][0].record(stream)
+            for c in range(nch):
+                dw.run_chunk(c, stream)
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - w0
+    dw.check_status()
+    return [a.elapsed_time(b) for a, b in ev], clk.summary(), wall
+
+
+def fractions(counts, comp_ms, peak_tf):
+    """Attention and score + top-k flops per second against the bf16 peak."""
+    attn_tf = counts["attn_flops"] / (comp_ms["attention"] * 1e-3) / 1e12
+    st_tf = (counts["score_flops"] / (comp_ms["score_topk"] * 1e-3) / 1e12
+             if counts["score_flops"] else None)
+    return attn_tf, st_tf
+
+
+def measure_config(name, tile, dev, stream, flush, steps, peak_tf, clock_index):
+    """One `configs` entry: the workload's own step timed as the headline step is."""
+    import torch
+    from deepseek_v4_sparse_ratio_gb300 import inputs
+    from deepseek_v4_sparse_ratio_gb300.runner import DeviceWorkload
+    wl = inputs.draw(inputs.workload(name))
+    tile = tile or wl.tile_rows[0]
+    dw = DeviceWorkload(wl, tile_rows=tile, device=dev)
+    snap = dw.state.snapshot()
+    step_ms, clocks, _ = time_steps(dw, wl, snap, flush, stream, steps, 3, clock_index)
+    ms = statistics.mean(step_ms)
+    comp = component_times(dw, wl, tile, snap, flush, stream, 3)
+    counts = work_counts(wl)
+    attn_tf, st_tf = fractions(counts, comp, peak_tf)
+    out = {"ms_per_step": ms, "value": wl.total / (ms * 1e-3), "unit": UNIT,
+           "tokens_per_step": wl.total, "chunks": list(wl.chunks), "context": wl.end,
+           "index_topk": wl.index_topk, "tile_rows": tile, "steps": steps, "warmup": 3,
+           "components_ms": comp, "attention_frac": attn_tf / peak_tf,
+           "score_topk_frac": st_tf / peak_tf if st_tf else None,
+           "score_flops": counts["score_flops"], "attn_flops": counts["attn_flops"],
+           "score_scratch_bytes": score_scratch_bytes(wl, tile), "clocks": clocks,
+           "launches_per_step": step_launches(wl, tile)}
+    del dw
+    torch.cuda.empty_cache()
+    return out
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -307,6 +440,7 @@ def main():
     ap.add_argument("--tile-rows", type=int, default=0)
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the other workloads")
     ap.add_argument("--ref-rows", type=int, default=16)
     args = ap.parse_args()
     if args.impl == "reference":
@@ -327,77 +461,31 @@ def main():
     wl = inputs.workload(args.workload)
     wl.seed += 1000 * rank   # independent replica per rank
     inputs.draw(wl)
-    T = wl.chunks[0]
-    assert len(wl.chunks) == 1 and wl.off0 > 0, "bench workloads are single-chunk with a prefix"
+    T = wl.total
     tile = args.tile_rows or wl.tile_rows[0]
     dw = DeviceWorkload(wl, tile_rows=tile, device=dev)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(512 * 2 ** 20 // 4, dtype=torch.float32, device=dev)
     snap = dw.state.snapshot()
     counts = work_counts(wl)
-    r = wl.ratio
-    n = (wl.off0 + T) // r
-
-    def step():
-        dw.state.restore(snap)
-        dw.run_chunk(0, stream)
-
-    # ---- warm-up
-    for _ in range(args.warmup):
-        flush.zero_()
-        step()
-    torch.cuda.synchronize()
-    dw.check_status()
+    n = wl.end // wl.ratio
 
     # ---- timed steps (device events around each step; L2 flushed between)
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
-          for _ in range(args.steps)]
     barrier(world)
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        w0 = time.perf_counter()
-        for i in range(args.steps):
-            flush.zero_()
-            ev[i][0].record(stream)
-            step()
-            ev[i][1].record(stream)
-        torch.cuda.synchronize()
-        wall = time.perf_counter() - w0
+    step_ms, clocks, wall = time_steps(dw, wl, snap, flush, stream, args.steps, args.warmup, local)
     barrier(world)
-    dw.check_status()
-    step_ms = [a.elapsed_time(b) for a, b in ev]
     ms = max_over_ranks(sum(step_ms) / len(step_ms), world, dev)
     value = job_throughput(T, world, ms)
 
     # ---- per-component times: the same calls one ABI entry point at a time
-    comp = {"pool": [], "score_topk": [], "attention": []}
-    s, off, k = 0, wl.off0, wl.index_topk
-    for i in range(max(3, args.steps // 2)):
-        flush.zero_()
-        dw.state.restore(snap)
-        e = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
-        e[0].record(stream)
-        B.dsa_pool_append(dw.state, dw.raw_kv[off - dw.raw_start:], dw.raw_ik, T, off, r, stream)
-        e[1].record(stream)
-        B.dsa_index_score_topk(dw.q_idx, dw.w, dw.state.pooled_ik, n, T, off, r, k, tile,
-                               dw.scratch, dw.sel, dw.status, stream)
-        e[2].record(stream)
-        B.dsa_window_sparse_attn(dw.q, dw.raw_kv, dw.raw_start, dw.state.pooled_kv, n, dw.sel, k,
-                                 T, off, r, wl.window, dw.scale, dw.out, dw.status, stream)
-        e[3].record(stream)
-        torch.cuda.synchronize()
-        if i >= 1:
-            comp["pool"].append(e[0].elapsed_time(e[1]))
-            comp["score_topk"].append(e[1].elapsed_time(e[2]))
-            comp["attention"].append(e[2].elapsed_time(e[3]))
-    comp_ms = {key: statistics.mean(v) for key, v in comp.items()}
-    dw.check_status()
+    comp_ms = component_times(dw, wl, tile, snap, flush, stream, max(3, args.steps // 2))
 
     # ---- end to end through the ABI with host buffers (pinned): dsa_prefill_chunk_host
     # copies the inputs in, runs the path and copies the selection and output back,
     # overlapping the copies with the kernels on a second stream; all of it is timed
     e2e = None
-    if not args.no_e2e:
+    if not args.no_e2e and len(wl.chunks) == 1:
+        off, k = wl.off0, wl.index_topk
         pin = lambda t: t.contiguous().pin_memory()
         raw_h = pin(torch.cat([wl.t["prefix_win"], wl.t["raw_kv"]], 0))
         host = {"raw_ik": pin(wl.t["raw_ik"]), "q_idx": pin(wl.t["q_idx"]),
@@ -410,17 +498,18 @@ def main():
         d2h = out_h.numel() * out_h.element_size() + sel_h.numel() * sel_h.element_size()
 
         def e2e_step():
-            dw.state.restore(snap)
             B.dsa_prefill_chunk_host(dw.state, ws, raw_h, dw.raw_start, host["raw_ik"],
                                      host["q_idx"], host["w"], host["q"], T, off, k, wl.window,
                                      dw.scale, tile, sel_h, out_h, dw.status, stream, side)
 
         for _ in range(3):
+            dw.state.restore(snap)
             e2e_step()
         torch.cuda.synchronize()
         ee = []
         for i in range(max(3, args.steps // 10)):
             flush.zero_()
+            dw.state.restore(snap)
             a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a.record(stream)
             e2e_step()
@@ -437,12 +526,10 @@ def main():
     peaks, src = load_peaks()
     # every kernel here is timed alone (one ABI call between events): burst peaks
     peak_tf, peak_bw = peaks["bf16_tflops"], peaks["hbm_gbs"]
-    attn_tf = counts["attn_flops"] / (comp_ms["attention"] * 1e-3) / 1e12
-    st_tf = counts["score_flops"] / (comp_ms["score_topk"] * 1e-3) / 1e12
+    attn_tf, st_tf = fractions(counts, comp_ms, peak_tf)
     attn_traffic = ncu_traffic("attn_kernel", args.workload)
-    skip = n <= wl.index_topk
     launches_per_step = step_launches(wl, tile)
-    if skip:
+    if st_tf is None:
         # nothing is scored on the skip path: a selection fill only
         st_roof = {"kernel": "fill_selection_kernel (dsa_index_score_topk skip path: every "
                              "pooled row fits in index_topk)",
@@ -451,7 +538,8 @@ def main():
         # the fused indexer step: score kernel + top-k kernel of each tile
         st_traffic = ncu_traffic("score_kernel", args.workload)
         if st_traffic is not None:
-            st_traffic += ncu_traffic("topk_kernel", args.workload)
+            tk = ncu_traffic("topk_kernel", args.workload)
+            st_traffic = st_traffic + tk if tk is not None else None
         st_roof = {"kernel": "score_kernel + topk_kernel (dsa_index_score_topk)",
                    "bound": "tensor", "achieved": st_tf, "peak": peak_tf, "unit": "TFLOP/s",
                    "frac": st_tf / peak_tf, "traffic": st_traffic,
@@ -475,13 +563,24 @@ def main():
                      "ms_per_launch": comp_ms["attention"]},
         "score_topk_roofline": st_roof,
         "components_ms": comp_ms,
+        "score_scratch_bytes": score_scratch_bytes(wl, tile),
         "gpu_launches": args.steps * launches_per_step,
-        "clocks": clk.summary(),
+        "clocks": clocks,
         "wall_s_timed_region": wall,
     }
     if e2e:
         line["e2e"] = e2e
-    if rank == 0 and not args.no_cpu:
+    if not args.no_configs and world == 1:
+        del dw
+        torch.cuda.empty_cache()
+        line["configs"] = {}
+        for name, ctile in EXTRA_CONFIGS:
+            if name == args.workload:
+                continue
+            line["configs"][name] = measure_config(name, ctile, dev, stream, flush,
+                                                   max(3, min(20, args.steps // 15)), peak_tf,
+                                                   local)
+    if rank == 0 and not args.no_cpu and len(wl.chunks) == 1 and wl.off0 > 0:
         line["cpu_baseline"] = cpu_baseline(wl)
     if rank == 0:
         print(json.dumps(line), flush=True)

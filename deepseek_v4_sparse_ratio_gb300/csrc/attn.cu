@@ -44,6 +44,7 @@
 #include <math.h>
 
 #include <algorithm>
+#include <mutex>
 
 #include "common.cuh"
 
@@ -629,13 +630,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         tmem_wait_st();
                     }
                 }
-                // this thread's 32 heads of the P^T row for key kl: 4 swizzled 16-byte pieces
+                // this thread's 32 heads of the P^T row for key kl: 4 swizzled 16-byte pieces.
+                // The sums take P as rounded to bf16, the values the PV MMA multiplies, so
+                // numerator and denominator weigh every key alike.
                 {
                     float pr[32];
 #pragma unroll
                     for (int h = 0; h < 32; ++h) pr[h] = valid ? ex2(xv[h]) : 0.0f;
-#pragma unroll
-                    for (int h = 0; h < 32; ++h) l[h] += pr[h];
                     uint8_t *prow = sP + kl * 128;
 #pragma unroll
                     for (int q = 0; q < 4; ++q) {
@@ -645,6 +646,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                             const __nv_bfloat162 v =
                                 __floats2bfloat162_rn(pr[8 * q + 2 * e], pr[8 * q + 2 * e + 1]);
                             pk[e] = *reinterpret_cast<const uint32_t *>(&v);
+                            l[8 * q + 2 * e] += bf16lo(pk[e]);
+                            l[8 * q + 2 * e + 1] += bf16hi(pk[e]);
                         }
                         *reinterpret_cast<uint4 *>(prow + (((4 * hh + q) ^ (kl & 7)) << 4)) =
                             make_uint4(pk[0], pk[1], pk[2], pk[3]);
@@ -814,7 +817,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 constexpr int kSplitN = 8;
 
 template <int kSplit>
-int prepare_attention() {
+int prepare_attention_kernel() {
     // the setmaxnreg split is only safe with the launch allocation it assumes
     cudaFuncAttributes fa;
     if (cudaFuncGetAttributes(&fa, attn_kernel<kSplit>) != cudaSuccess ||
@@ -846,30 +849,59 @@ cudaLaunchAttribute cluster_attr() {
 
 }  // namespace
 
-int launch_attention(const void *q, const void *raw_kv, int64_t raw_start, int64_t raw_rows,
-                     const void *pooled_kv, int64_t n, const int32_t *sel, int32_t k,
-                     int64_t chunk, int64_t offset, int32_t ratio, int32_t window, float scale,
-                     void *out, int32_t *status, cudaStream_t s) {
-    (void)raw_rows;
-    static bool checked = false;
-    static bool split_ok = false;
-    if (!checked) {
-        if (prepare_attention<1>() != DSA_OK || prepare_attention<kSplitN>() != DSA_OK)
-            return DSA_ERR_CUDA;
-        // can a cluster of kSplitN whole-SM CTAs be resident at all?
-        int nc = 0;
-        cudaLaunchConfig_t cfg = split_config(kSplitN, nullptr);
-        cudaLaunchAttribute at = cluster_attr();
-        cfg.attrs = &at;
-        cfg.numAttrs = 1;
-        split_ok = cudaOccupancyMaxActiveClusters(&nc, attn_kernel<kSplitN>, &cfg) == cudaSuccess &&
-                   nc > 0;
-        (void)cudaGetLastError();
-        checked = true;
+namespace {
+
+// Per-device one-time set-up: the raised shared-memory limit of both kernel
+// instances, and whether a cluster of kSplitN whole-SM CTAs can be resident.
+struct AttnSetup {
+    bool done = false;
+    int rc = DSA_OK;
+    bool split_ok = false;
+};
+std::mutex g_attn_mu;
+AttnSetup g_attn_setup[kMaxDevices];
+
+int attention_setup(bool *split_ok) {
+    const int dev = current_device();
+    if (dev < 0) return DSA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_attn_mu);
+    AttnSetup &st = g_attn_setup[dev];
+    if (!st.done) {
+        st.rc = (prepare_attention_kernel<1>() == DSA_OK &&
+                 prepare_attention_kernel<kSplitN>() == DSA_OK)
+                    ? DSA_OK
+                    : DSA_ERR_CUDA;
+        if (st.rc == DSA_OK) {
+            int nc = 0;
+            cudaLaunchConfig_t cfg = split_config(kSplitN, nullptr);
+            cudaLaunchAttribute at = cluster_attr();
+            cfg.attrs = &at;
+            cfg.numAttrs = 1;
+            st.split_ok = cudaOccupancyMaxActiveClusters(&nc, attn_kernel<kSplitN>, &cfg) ==
+                              cudaSuccess &&
+                          nc > 0;
+            (void)cudaGetLastError();
+        }
+        st.done = true;
     }
-    CUtensorMap tm_q;
-    if (!make_tmap_bf16(&tm_q, q, kD, static_cast<uint64_t>(chunk) * kH, kD * 2, 64, 64))
+    *split_ok = st.split_ok;
+    return st.rc;
+}
+
+}  // namespace
+
+int prepare_attention(const void *q, int64_t chunk, AttnPlan *plan) {
+    int rc = attention_setup(&plan->split_ok);
+    if (rc != DSA_OK) return rc;
+    if (!make_tmap_bf16(&plan->tm_q, q, kD, static_cast<uint64_t>(chunk) * kH, kD * 2, 64, 64))
         return DSA_ERR_CUDA;
+    return DSA_OK;
+}
+
+int enqueue_attention(const AttnPlan &plan, const void *raw_kv, int64_t raw_start,
+                      const void *pooled_kv, int64_t n, const int32_t *sel, int32_t k,
+                      int64_t chunk, int64_t offset, int32_t ratio, int32_t window, float scale,
+                      void *out, int32_t *status, cudaStream_t s) {
     AttnParams p;
     p.out = static_cast<__nv_bfloat16 *>(out);
     p.raw_kv = static_cast<const __nv_bfloat16 *>(raw_kv);
@@ -890,18 +922,18 @@ int launch_attention(const void *q, const void *raw_kv, int64_t raw_start, int64
     const int64_t nv = std::min(n, (t_last + 1) / ratio);
     const int64_t nwin = t_last - std::max<int64_t>(0, t_last - window + 1) + 1;
     const int64_t nb = (nwin + 127) / 128 + (std::min<int64_t>(k, nv) + 127) / 128;
-    if (split_ok && chunk * kSplitN <= sms && nb > 1) {
+    if (plan.split_ok && chunk * kSplitN <= sms && nb > 1) {
         // few tokens: a cluster per token spreads its key blocks over kSplitN SMs
         cudaLaunchConfig_t cfg = split_config(static_cast<unsigned>(chunk * kSplitN), s);
         cudaLaunchAttribute at = cluster_attr();
         cfg.attrs = &at;
         cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, attn_kernel<kSplitN>, tm_q, p) != cudaSuccess)
+        if (cudaLaunchKernelEx(&cfg, attn_kernel<kSplitN>, plan.tm_q, p) != cudaSuccess)
             return DSA_ERR_CUDA;
         return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
     }
     const int grid = static_cast<int>(std::min<int64_t>(chunk, sms));
-    attn_kernel<1><<<grid, kAttnThreads, kAttnSmem, s>>>(tm_q, p);
+    attn_kernel<1><<<grid, kAttnThreads, kAttnSmem, s>>>(plan.tm_q, p);
     return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
@@ -936,7 +968,10 @@ extern "C" int dsa_window_sparse_attn(const void *q, const void *raw_kv, int64_t
     int rc = check_attention(q, raw_kv, raw_start, raw_rows, pooled_kv, n_pooled, sel, index_topk,
                              chunk, offset, ratio, window, scale, out);
     if (rc != DSA_OK) return rc;
-    return launch_attention(q, raw_kv, raw_start, raw_rows, pooled_kv, n_pooled, sel, index_topk,
-                            chunk, offset, ratio, window, scale, out, dev_status,
-                            static_cast<cudaStream_t>(stream));
+    AttnPlan plan;
+    rc = prepare_attention(q, chunk, &plan);
+    if (rc != DSA_OK) return rc;
+    return enqueue_attention(plan, raw_kv, raw_start, pooled_kv, n_pooled, sel, index_topk, chunk,
+                             offset, ratio, window, scale, out, dev_status,
+                             static_cast<cudaStream_t>(stream));
 }

@@ -40,26 +40,50 @@ bool make_tmap_bf16(CUtensorMap *map, const void *base, uint64_t inner, uint64_t
 
 int sm_count();
 
+// One-time set-up (raised shared-memory limits, occupancy probes) is per device:
+// each launcher keeps it in a table indexed by the current device's ordinal.
+constexpr int kMaxDevices = 64;
+int current_device();  // the current device's ordinal, or -1 when unusable
+
+// Each step is split in two: prepare_* does everything that can fail short of a
+// launch (argument-derived tensor maps, per-device set-up) and enqueue_* only
+// launches. The whole-chunk calls prepare every step before enqueuing any, so a
+// rejected call enqueues nothing.
+
 // Launchers (stream-ordered, no host synchronization). Each returns DSA_OK or
 // DSA_ERR_CUDA; arguments are validated by the caller.
 int launch_pool_append(const dsa_pool_state &st, const void *raw_kv, const void *raw_ik,
                        int64_t chunk, int64_t offset, cudaStream_t s);
 int launch_fill_selection(int32_t *sel, int64_t rows, int32_t k, int64_t offset, int64_t n,
                           int32_t ratio, cudaStream_t s);
-// launch_score_tile also writes each row's per-segment score range into the
-// row's selection entries when k >= 2 x segments (sel may be null) and reports
-// the segment count in *nseg_rng (0 when it did not); launch_topk_tile then
-// takes the range from there (nseg_rng > 0) instead of a pass over the scores.
-int launch_score_tile(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const float *w,
-                      int64_t n, int64_t offset, int32_t ratio, int64_t r0, int64_t R,
-                      float *scores, int64_t stride, int32_t *sel, int32_t k, int *nseg_rng,
-                      int32_t *status, cudaStream_t s);
-int launch_topk_tile(const float *scores, int64_t stride, int64_t n, int64_t offset,
-                     int32_t ratio, int64_t r0, int64_t R, int32_t k, int32_t nseg_rng,
-                     int32_t *sel, int32_t *status, cudaStream_t s);
-int launch_attention(const void *q, const void *raw_kv, int64_t raw_start, int64_t raw_rows,
-                     const void *pooled_kv, int64_t n, const int32_t *sel, int32_t k,
-                     int64_t chunk, int64_t offset, int32_t ratio, int32_t window, float scale,
-                     void *out, int32_t *status, cudaStream_t s);
+
+// Score + top-k of one chunk (steps b, c): the full path when n > k.
+struct ScoreTopkPlan {
+    bool full = false;
+    CUtensorMap tm_q, tm_k;
+};
+int check_score_topk(const void *q_idx, const float *w, const void *pooled_ik, int64_t n,
+                     int64_t chunk, int64_t offset, int32_t ratio, int32_t k, int64_t tile_rows,
+                     const void *scratch, size_t scratch_bytes, const int32_t *sel);
+int prepare_score_topk(const void *q_idx, const void *pooled_ik, int64_t n, int64_t chunk,
+                       int32_t k, ScoreTopkPlan *plan);
+int enqueue_score_topk(const ScoreTopkPlan &plan, const float *w, int64_t n, int64_t chunk,
+                       int64_t offset, int32_t ratio, int32_t k, int64_t tile_rows,
+                       void *scratch, int32_t *sel, int32_t *status, cudaStream_t s);
+
+// Window + selected attention (step d).
+struct AttnPlan {
+    CUtensorMap tm_q;
+    bool split_ok = false;  // the cluster launch of the split mode can be resident
+};
+int check_attention(const void *q, const void *raw_kv, int64_t raw_start, int64_t raw_rows,
+                    const void *pooled_kv, int64_t n, const int32_t *sel, int32_t k,
+                    int64_t chunk, int64_t offset, int32_t ratio, int32_t window, float scale,
+                    const void *out);
+int prepare_attention(const void *q, int64_t chunk, AttnPlan *plan);
+int enqueue_attention(const AttnPlan &plan, const void *raw_kv, int64_t raw_start,
+                      const void *pooled_kv, int64_t n, const int32_t *sel, int32_t k,
+                      int64_t chunk, int64_t offset, int32_t ratio, int32_t window, float scale,
+                      void *out, int32_t *status, cudaStream_t s);
 
 }  // namespace dsa

@@ -11,19 +11,6 @@
 #include "common.cuh"
 
 namespace dsa {
-int check_score_topk(const void *q_idx, const float *w, const void *pooled_ik, int64_t n,
-                     int64_t chunk, int64_t offset, int32_t ratio, int32_t k, int64_t tile_rows,
-                     const void *scratch, size_t scratch_bytes, const int32_t *sel);
-int run_score_topk(const void *q_idx, const float *w, const void *pooled_ik, int64_t n,
-                   int64_t chunk, int64_t offset, int32_t ratio, int32_t k, int64_t tile_rows,
-                   void *scratch, int32_t *sel, int32_t *status, cudaStream_t s);
-int check_attention(const void *q, const void *raw_kv, int64_t raw_start, int64_t raw_rows,
-                    const void *pooled_kv, int64_t n, const int32_t *sel, int32_t k,
-                    int64_t chunk, int64_t offset, int32_t ratio, int32_t window, float scale,
-                    const void *out);
-}  // namespace dsa
-
-namespace dsa {
 namespace {
 
 // Every argument of one chunk's path, checked before anything is enqueued.
@@ -53,25 +40,29 @@ int check_prefill(const dsa_pool_state *st, const void *raw_kv, int64_t raw_star
                            chunk, offset, ratio, window, scale, out);
 }
 
-// Pool/append + score/top-k for one chunk on stream s (arguments already checked);
-// advances the host-side state.
-int enqueue_pool_and_select(dsa_pool_state *st, const void *raw_kv, int64_t raw_start,
-                            const void *raw_ik, const void *q_idx, const float *w,
-                            int64_t chunk, int64_t offset, int32_t index_topk,
+// The host-side state after this chunk's append. Written only once every launch
+// of the call has been enqueued: a call that returns an error leaves it as it was.
+void advance_state(dsa_pool_state *st, int64_t end) {
+    st->n_pooled_kv = st->n_pooled_ik = end / st->ratio;
+    st->n_tokens = end;
+    st->n_rem = static_cast<int32_t>(end % st->ratio);
+}
+
+// Pool/append + score/top-k for one chunk on stream s (arguments checked, plan
+// prepared); the state is advanced by the caller.
+int enqueue_pool_and_select(const dsa_pool_state *st, const ScoreTopkPlan &plan,
+                            const void *raw_kv, int64_t raw_start, const void *raw_ik,
+                            const float *w, int64_t chunk, int64_t offset, int32_t index_topk,
                             int64_t tile_rows, void *scratch, int32_t *sel, int32_t *status,
                             cudaStream_t s) {
     const int32_t ratio = st->ratio;
-    const int64_t end = offset + chunk;
-    const int64_t n = end / ratio;
+    const int64_t n = (offset + chunk) / ratio;
     const void *chunk_kv =
         static_cast<const uint8_t *>(raw_kv) + (offset - raw_start) * int64_t{kD} * 2;
     int rc = launch_pool_append(*st, chunk_kv, raw_ik, chunk, offset, s);
     if (rc != DSA_OK) return rc;
-    st->n_pooled_kv = st->n_pooled_ik = n;
-    st->n_tokens = end;
-    st->n_rem = static_cast<int32_t>(end % ratio);
-    return run_score_topk(q_idx, w, st->pooled_ik, n, chunk, offset, ratio, index_topk,
-                          tile_rows, scratch, sel, status, s);
+    return enqueue_score_topk(plan, w, n, chunk, offset, ratio, index_topk, tile_rows, scratch,
+                              sel, status, s);
 }
 
 }  // namespace
@@ -87,13 +78,23 @@ extern "C" int dsa_prefill_chunk(dsa_pool_state *st, const void *raw_kv, int64_t
     int rc = check_prefill(st, raw_kv, raw_start, raw_rows, raw_ik, q_idx, w, q, chunk, offset,
                            index_topk, window, scale, tile_rows, scratch, scratch_bytes, sel, out);
     if (rc != DSA_OK) return rc;
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    rc = enqueue_pool_and_select(st, raw_kv, raw_start, raw_ik, q_idx, w, chunk, offset,
-                                 index_topk, tile_rows, scratch, sel, dev_status, s);
+    const int64_t end = offset + chunk;
+    const int64_t n = end / st->ratio;
+    // everything that can fail short of a launch, before the first launch
+    ScoreTopkPlan splan;
+    AttnPlan aplan;
+    rc = prepare_score_topk(q_idx, st->pooled_ik, n, chunk, index_topk, &splan);
+    if (rc == DSA_OK) rc = prepare_attention(q, chunk, &aplan);
     if (rc != DSA_OK) return rc;
-    return launch_attention(q, raw_kv, raw_start, raw_rows, st->pooled_kv, st->n_pooled_kv, sel,
-                            index_topk, chunk, offset, st->ratio, window, scale, out, dev_status,
-                            s);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    rc = enqueue_pool_and_select(st, splan, raw_kv, raw_start, raw_ik, w, chunk, offset,
+                                 index_topk, tile_rows, scratch, sel, dev_status, s);
+    if (rc == DSA_OK)
+        rc = enqueue_attention(aplan, raw_kv, raw_start, st->pooled_kv, n, sel, index_topk, chunk,
+                               offset, st->ratio, window, scale, out, dev_status, s);
+    if (rc != DSA_OK) return rc;
+    advance_state(st, end);
+    return DSA_OK;
 }
 
 namespace {
@@ -129,35 +130,9 @@ extern "C" int dsa_prefill_chunk_host(dsa_pool_state *st, const dsa_prefill_work
                            ws->q, chunk, offset, index_topk, window, scale, tile_rows,
                            ws->scratch, ws->scratch_bytes, ws->sel, ws->out);
     if (rc != DSA_OK) return rc;
-
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
-    cudaStream_t c = static_cast<cudaStream_t>(copy_stream);
-    const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
+    const int64_t end = offset + chunk;
+    const int64_t n = end / st->ratio;
     const size_t q_row = size_t{kH} * kD * 2;  // bytes of one query row (all heads)
-    Events ev;
-    cudaEvent_t in_done = ev.make(), q_done = ev.make(), sel_done = ev.make(), all_done = ev.make();
-    if (!in_done || !q_done || !sel_done || !all_done) return DSA_ERR_CUDA;
-    bool ok = true;
-    // inputs of pooling and the indexer on the compute stream; the query rows follow on
-    // the copy stream and land while pooling and the indexer run
-    ok = ok && cudaMemcpyAsync(ws->raw_kv, raw_kv_h, size_t(raw_rows) * kD * 2, h2d, s) == cudaSuccess;
-    ok = ok && cudaMemcpyAsync(ws->raw_ik, raw_ik_h, size_t(chunk) * kDI * 2, h2d, s) == cudaSuccess;
-    ok = ok && cudaMemcpyAsync(ws->q_idx, q_idx_h, size_t(chunk) * kHI * kDI * 2, h2d, s) == cudaSuccess;
-    ok = ok && cudaMemcpyAsync(ws->w, w_h, size_t(chunk) * kHI * 4, h2d, s) == cudaSuccess;
-    ok = ok && cudaEventRecord(in_done, s) == cudaSuccess;
-    ok = ok && cudaStreamWaitEvent(c, in_done, 0) == cudaSuccess;
-    ok = ok && cudaMemcpyAsync(ws->q, q_h, size_t(chunk) * q_row, h2d, c) == cudaSuccess;
-    ok = ok && cudaEventRecord(q_done, c) == cudaSuccess;
-    if (!ok) return DSA_ERR_CUDA;
-
-    rc = enqueue_pool_and_select(st, ws->raw_kv, raw_start, ws->raw_ik, ws->q_idx, ws->w, chunk,
-                                 offset, index_topk, tile_rows, ws->scratch, ws->sel, dev_status, s);
-    if (rc != DSA_OK) return rc;
-    ok = ok && cudaEventRecord(sel_done, s) == cudaSuccess;
-    ok = ok && cudaStreamWaitEvent(c, sel_done, 0) == cudaSuccess;
-    ok = ok && cudaMemcpyAsync(sel_h, ws->sel, size_t(chunk) * index_topk * 4, d2h, c) == cudaSuccess;
-    ok = ok && cudaStreamWaitEvent(s, q_done, 0) == cudaSuccess;
-    if (!ok) return DSA_ERR_CUDA;
 
     // attention in row slices; each slice's output goes back while the next computes.
     // Slices shrink towards the end (whole waves of one row per SM where possible), so
@@ -178,19 +153,59 @@ extern "C" int dsa_prefill_chunk_host(dsa_pool_state *st, const dsa_prefill_work
         }
         cuts[ncut++] = chunk;
     }
+    // every step's plan (tensor maps, per-device set-up) and every event, before the
+    // first copy or launch
+    ScoreTopkPlan splan;
+    AttnPlan aplan[8];
+    rc = prepare_score_topk(ws->q_idx, st->pooled_ik, n, chunk, index_topk, &splan);
+    for (int ci = 0; ci < ncut && rc == DSA_OK; ++ci) {
+        const int64_t r0 = ci ? cuts[ci - 1] : 0;
+        rc = prepare_attention(static_cast<const uint8_t *>(ws->q) + r0 * q_row, cuts[ci] - r0,
+                               &aplan[ci]);
+    }
+    if (rc != DSA_OK) return rc;
+    Events ev;
+    cudaEvent_t in_done = ev.make(), q_done = ev.make(), sel_done = ev.make(), all_done = ev.make();
+    cudaEvent_t slice_done[8] = {};
+    bool have_events = in_done && q_done && sel_done && all_done;
+    for (int ci = 0; ci < ncut; ++ci) have_events = have_events && (slice_done[ci] = ev.make());
+    if (!have_events) return DSA_ERR_CUDA;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaStream_t c = static_cast<cudaStream_t>(copy_stream);
+    const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
+    bool ok = true;
+    // inputs of pooling and the indexer on the compute stream; the query rows follow on
+    // the copy stream and land while pooling and the indexer run
+    ok = ok && cudaMemcpyAsync(ws->raw_kv, raw_kv_h, size_t(raw_rows) * kD * 2, h2d, s) == cudaSuccess;
+    ok = ok && cudaMemcpyAsync(ws->raw_ik, raw_ik_h, size_t(chunk) * kDI * 2, h2d, s) == cudaSuccess;
+    ok = ok && cudaMemcpyAsync(ws->q_idx, q_idx_h, size_t(chunk) * kHI * kDI * 2, h2d, s) == cudaSuccess;
+    ok = ok && cudaMemcpyAsync(ws->w, w_h, size_t(chunk) * kHI * 4, h2d, s) == cudaSuccess;
+    ok = ok && cudaEventRecord(in_done, s) == cudaSuccess;
+    ok = ok && cudaStreamWaitEvent(c, in_done, 0) == cudaSuccess;
+    ok = ok && cudaMemcpyAsync(ws->q, q_h, size_t(chunk) * q_row, h2d, c) == cudaSuccess;
+    ok = ok && cudaEventRecord(q_done, c) == cudaSuccess;
+    if (!ok) return DSA_ERR_CUDA;
+
+    rc = enqueue_pool_and_select(st, splan, ws->raw_kv, raw_start, ws->raw_ik, ws->w, chunk,
+                                 offset, index_topk, tile_rows, ws->scratch, ws->sel, dev_status, s);
+    if (rc != DSA_OK) return rc;
+    ok = ok && cudaEventRecord(sel_done, s) == cudaSuccess;
+    ok = ok && cudaStreamWaitEvent(c, sel_done, 0) == cudaSuccess;
+    ok = ok && cudaMemcpyAsync(sel_h, ws->sel, size_t(chunk) * index_topk * 4, d2h, c) == cudaSuccess;
+    ok = ok && cudaStreamWaitEvent(s, q_done, 0) == cudaSuccess;
+    if (!ok) return DSA_ERR_CUDA;
+
     for (int ci = 0; ci < ncut; ++ci) {
         const int64_t r0 = ci ? cuts[ci - 1] : 0;
         const int64_t rows = cuts[ci] - r0;
-        rc = launch_attention(static_cast<const uint8_t *>(ws->q) + r0 * q_row, ws->raw_kv,
-                              raw_start, raw_rows, st->pooled_kv, st->n_pooled_kv,
-                              ws->sel + r0 * index_topk, index_topk, rows, offset + r0,
-                              st->ratio, window, scale,
-                              static_cast<uint8_t *>(ws->out) + r0 * q_row, dev_status, s);
+        rc = enqueue_attention(aplan[ci], ws->raw_kv, raw_start, st->pooled_kv, n,
+                               ws->sel + r0 * index_topk, index_topk, rows, offset + r0,
+                               st->ratio, window, scale,
+                               static_cast<uint8_t *>(ws->out) + r0 * q_row, dev_status, s);
         if (rc != DSA_OK) return rc;
-        cudaEvent_t slice_done = ev.make();
-        if (!slice_done) return DSA_ERR_CUDA;
-        ok = ok && cudaEventRecord(slice_done, s) == cudaSuccess;
-        ok = ok && cudaStreamWaitEvent(c, slice_done, 0) == cudaSuccess;
+        ok = ok && cudaEventRecord(slice_done[ci], s) == cudaSuccess;
+        ok = ok && cudaStreamWaitEvent(c, slice_done[ci], 0) == cudaSuccess;
         ok = ok && cudaMemcpyAsync(static_cast<uint8_t *>(out_h) + r0 * q_row,
                                    static_cast<const uint8_t *>(ws->out) + r0 * q_row,
                                    size_t(rows) * q_row, d2h, c) == cudaSuccess;
@@ -198,5 +213,7 @@ extern "C" int dsa_prefill_chunk_host(dsa_pool_state *st, const dsa_prefill_work
     }
     ok = ok && cudaEventRecord(all_done, c) == cudaSuccess;
     ok = ok && cudaStreamWaitEvent(s, all_done, 0) == cudaSuccess;
-    return ok ? DSA_OK : DSA_ERR_CUDA;
+    if (!ok) return DSA_ERR_CUDA;
+    advance_state(st, end);
+    return DSA_OK;
 }

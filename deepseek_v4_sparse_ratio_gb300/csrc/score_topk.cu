@@ -35,6 +35,8 @@
 // ascending, taking equal scores lowest index first.
 #include <math.h>
 
+#include <cudaTypedefs.h>
+
 #include <algorithm>
 #include <mutex>
 
@@ -688,13 +690,6 @@ int launch_score_tile(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const fl
                       int64_t offset, int32_t ratio, int64_t r0, int64_t R, float *scores,
                       int64_t stride, int32_t *sel, int32_t k, int *nseg_rng, int32_t *status,
                       cudaStream_t s) {
-    static bool attr_set = false;
-    if (!attr_set) {
-        if (cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kScoreSmem) != cudaSuccess)
-            return DSA_ERR_CUDA;
-        attr_set = true;
-    }
     const int sms = std::max(1, sm_count());
     ScoreParams p;
     p.w = w;
@@ -756,22 +751,52 @@ int check_score_topk(const void *q_idx, const float *w, const void *pooled_ik, i
     return DSA_OK;
 }
 
-int run_score_topk(const void *q_idx, const float *w, const void *pooled_ik, int64_t n,
-                   int64_t chunk, int64_t offset, int32_t ratio, int32_t k, int64_t tile_rows,
-                   void *scratch, int32_t *sel, int32_t *status, cudaStream_t s) {
-    if (n == 0 || n <= k) return launch_fill_selection(sel, chunk, k, offset, n, ratio, s);
-    CUtensorMap tm_q, tm_k;
-    if (!make_tmap_bf16(&tm_q, q_idx, kDI, static_cast<uint64_t>(chunk) * kHI, kDI * 2, 64, 256))
+namespace {
+
+// Per-device one-time set-up of the score kernel's raised shared-memory limit.
+std::mutex g_score_mu;
+int g_score_setup[kMaxDevices];  // 0 = not yet, else DSA_OK + 1 or the error
+
+int score_setup() {
+    const int dev = current_device();
+    if (dev < 0) return DSA_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_score_mu);
+    if (g_score_setup[dev] == 0) {
+        const bool ok = cudaFuncSetAttribute(score_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             kScoreSmem) == cudaSuccess;
+        g_score_setup[dev] = ok ? DSA_OK + 1 : DSA_ERR_CUDA;
+    }
+    return g_score_setup[dev] == DSA_OK + 1 ? DSA_OK : g_score_setup[dev];
+}
+
+}  // namespace
+
+int prepare_score_topk(const void *q_idx, const void *pooled_ik, int64_t n, int64_t chunk,
+                       int32_t k, ScoreTopkPlan *plan) {
+    plan->full = n > 0 && n > k;
+    if (!plan->full) return DSA_OK;
+    int rc = score_setup();
+    if (rc != DSA_OK) return rc;
+    if (!make_tmap_bf16(&plan->tm_q, q_idx, kDI, static_cast<uint64_t>(chunk) * kHI, kDI * 2,
+                        64, 256))
         return DSA_ERR_CUDA;
-    if (!make_tmap_bf16(&tm_k, pooled_ik, kDI, static_cast<uint64_t>(n), kDI * 2, 64, 128))
+    if (!make_tmap_bf16(&plan->tm_k, pooled_ik, kDI, static_cast<uint64_t>(n), kDI * 2, 64, 128))
         return DSA_ERR_CUDA;
+    return DSA_OK;
+}
+
+int enqueue_score_topk(const ScoreTopkPlan &plan, const float *w, int64_t n, int64_t chunk,
+                       int64_t offset, int32_t ratio, int32_t k, int64_t tile_rows,
+                       void *scratch, int32_t *sel, int32_t *status, cudaStream_t s) {
+    if (!plan.full) return launch_fill_selection(sel, chunk, k, offset, n, ratio, s);
     const int64_t stride = score_stride(n);
     float *scores = static_cast<float *>(scratch);
     for (int64_t r0 = 0; r0 < chunk; r0 += tile_rows) {
         const int64_t R = std::min(tile_rows, chunk - r0);
         int nseg_rng = 0;
-        int rc = launch_score_tile(tm_q, tm_k, w, n, offset, ratio, r0, R, scores, stride, sel, k,
-                                   &nseg_rng, status, s);
+        int rc = launch_score_tile(plan.tm_q, plan.tm_k, w, n, offset, ratio, r0, R, scores,
+                                   stride, sel, k, &nseg_rng, status, s);
         if (rc != DSA_OK) return rc;
         rc = launch_topk_tile(scores, stride, n, offset, ratio, r0, R, k, nseg_rng, sel, status, s);
         if (rc != DSA_OK) return rc;
@@ -796,8 +821,11 @@ extern "C" int dsa_index_score_topk(const void *q_idx, const float *w, const voi
     int rc = check_score_topk(q_idx, w, pooled_ik, n_pooled, chunk, offset, ratio, index_topk,
                               tile_rows, scratch, scratch_bytes, sel);
     if (rc != DSA_OK) return rc;
-    return run_score_topk(q_idx, w, pooled_ik, n_pooled, chunk, offset, ratio, index_topk,
-                          tile_rows, scratch, sel, dev_status, static_cast<cudaStream_t>(stream));
+    ScoreTopkPlan plan;
+    rc = prepare_score_topk(q_idx, pooled_ik, n_pooled, chunk, index_topk, &plan);
+    if (rc != DSA_OK) return rc;
+    return enqueue_score_topk(plan, w, n_pooled, chunk, offset, ratio, index_topk, tile_rows,
+                              scratch, sel, dev_status, static_cast<cudaStream_t>(stream));
 }
 
 // ------------------------------------------------------------------ no-allocation variant
@@ -810,23 +838,58 @@ namespace {
 
 __device__ __align__(256) static float g_static_scratch[DSA_STATIC_SCRATCH_BYTES / sizeof(float)];
 
-constexpr int kMaxDevices = 64;
-std::mutex g_static_mu;
-void *g_static_ptr[kMaxDevices] = {};
+// The current context's unique id, 0 when there is none yet or it cannot be read.
+// A device reset destroys the context together with the module that holds the
+// array, so a cached address is reused only while the id stays the same.
+unsigned long long current_context_id() {
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 4000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(fn);
+        fn = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &fn, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(fn);
+    });
+    CUcontext ctx = nullptr;
+    unsigned long long id = 0;
+    if (!get_current || !get_id || get_current(&ctx) != CUDA_SUCCESS || !ctx ||
+        get_id(ctx, &id) != CUDA_SUCCESS)
+        return 0;
+    return id;
+}
 
-// Device address of g_static_scratch on the current device, looked up once per
-// device (the host-side name of the array is not a device address).
+struct StaticScratch {
+    unsigned long long ctx_id = 0;
+    void *ptr = nullptr;
+};
+std::mutex g_static_mu;
+StaticScratch g_static[kMaxDevices];
+
+// Device address of g_static_scratch on the current device (the host-side name
+// of the array is only a stand-in, not a device address). Looked up on the first
+// call on a device, and again only if the device's context has changed since.
 int static_scratch(void **out) {
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return DSA_ERR_CUDA;
+    const int dev = current_device();
+    if (dev < 0) return DSA_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_static_mu);
-    if (!g_static_ptr[dev]) {
+    StaticScratch &c = g_static[dev];
+    const unsigned long long id = current_context_id();
+    if (!c.ptr || id == 0 || id != c.ctx_id) {
         void *ptr = nullptr;
         if (cudaGetSymbolAddress(&ptr, g_static_scratch) != cudaSuccess || !ptr)
             return DSA_ERR_CUDA;
-        g_static_ptr[dev] = ptr;
+        c.ptr = ptr;
+        c.ctx_id = current_context_id();
     }
-    *out = g_static_ptr[dev];
+    *out = c.ptr;
     return DSA_OK;
 }
 
@@ -849,6 +912,9 @@ extern "C" int dsa_index_score_topk_noalloc(const void *q_idx, const float *w,
         rc = static_scratch(&scratch);
         if (rc != DSA_OK) return rc;
     }
-    return run_score_topk(q_idx, w, pooled_ik, n_pooled, chunk, offset, ratio, index_topk,
-                          tile_rows, scratch, sel, dev_status, static_cast<cudaStream_t>(stream));
+    ScoreTopkPlan plan;
+    rc = prepare_score_topk(q_idx, pooled_ik, n_pooled, chunk, index_topk, &plan);
+    if (rc != DSA_OK) return rc;
+    return enqueue_score_topk(plan, w, n_pooled, chunk, offset, ratio, index_topk, tile_rows,
+                              scratch, sel, dev_status, static_cast<cudaStream_t>(stream));
 }

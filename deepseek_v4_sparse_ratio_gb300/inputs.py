@@ -99,10 +99,10 @@ def workload(name: str) -> Workload:
     if name == "two_chunks_4098":
         # a 4,098-token prompt in two chunks: [0,2048) then [2048,4098)
         return Workload(name, 1, [2048, 2050], 0, 0, index_topk=512, window=128,
-                        sample_rows=256, tile_rows=(2048, 512))
+                        tile_rows=(2048, 512))
     if name == "prompt_16k":
         return Workload(name, 2, [2048] * 8, 0, 0, index_topk=2048, window=128,
-                        sample_rows=64, tile_rows=(2048,))
+                        tile_rows=(2048, 512))
     if name == "ctx_128k":
         off = 131072 - 4096
         return Workload(name, 3, [4096], off, off // RATIO, index_topk=2048,

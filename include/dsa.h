@@ -26,9 +26,17 @@
  *     pointer after the call returns; the caller owns all memory.
  *   - `stream` is a cudaStream_t (NULL = legacy default stream). Work is
  *     enqueued asynchronously; host-side state (dsa_pool_state counters) is
- *     updated at enqueue time.
- *   - Every argument is validated before anything is enqueued. On any error
- *     the call returns a negative DSA_ERR_* code and changes nothing.
+ *     updated at enqueue time, after the call's last launch or copy has been
+ *     enqueued.
+ *   - Every argument is validated, and every host-side step that can fail
+ *     short of a launch (tensor-map encoding, per-device kernel set-up, event
+ *     creation) is done, before anything is enqueued. On any such error the
+ *     call returns a negative DSA_ERR_* code and changes nothing. The one
+ *     exception is a launch or copy that the CUDA runtime rejects after earlier
+ *     work of the same call was enqueued (DSA_ERR_CUDA; the context is then in
+ *     an error state): the host-side state is still unchanged, but device
+ *     memory written by the work already enqueued (for example the remainder
+ *     rows of the pooling step) may have changed.
  *   - `dev_status` (optional, may be NULL) is a device int32 the kernels set
  *     to a DSA_ERR_* code when a bounded wait expires (DSA_ERR_TIMEOUT) or a
  *     gathered index is out of range (DSA_ERR_BOUNDS, the access is skipped).
@@ -266,8 +274,8 @@ typedef struct dsa_prefill_workspace {
  *   The host buffers must stay alive and unmodified until then.
  * Errors: those of dsa_prefill_chunk; DSA_ERR_ARG for a null host pointer or
  * workspace, DSA_ERR_CAPACITY when the chunk, index_topk or raw rows exceed
- * the workspace; DSA_ERR_CUDA if an event, copy or launch fails (after the
- * first enqueue the pool state has been advanced).
+ * the workspace; DSA_ERR_CUDA if an event, copy or launch fails (the pool
+ * state is advanced only once everything has been enqueued).
  */
 int dsa_prefill_chunk_host(dsa_pool_state *st, const dsa_prefill_workspace *ws,
                            const void *raw_kv_h, int64_t raw_start, int64_t raw_rows,
@@ -299,8 +307,10 @@ int dsa_prefill_chunk_host(dsa_pool_state *st, const dsa_prefill_workspace *ws,
  *   otherwise DSA_ERR_SCRATCH is returned and nothing is enqueued (pick a
  *   smaller tile_rows; the selection does not depend on it).
  *   The first full-path call on a device looks up the array's device address
- *   (cudaGetSymbolAddress) on the current device; make that first call before
- *   any stream capture.
+ *   (cudaGetSymbolAddress) on the current device, and a later call looks it up
+ *   again only if the device's context has changed (after cudaDeviceReset);
+ *   make the first call on a device, and the first after a reset, before any
+ *   stream capture.
  *   All calls on a device share the one array and it keeps the last call's
  *   contents (nothing in it needs to start at zero). Calls whose work overlaps
  *   on the GPU -- on different streams, or from several threads -- race on it;

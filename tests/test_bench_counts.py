@@ -66,3 +66,20 @@ def test_launch_counts_match_the_launch_lists():
     assert bench.step_launches(inputs.workload("decode_128k"), 1) == 4
     assert bench.step_launches(inputs.workload("ctx_1m"), 1024) == 1 + 8 + 1
     assert bench.step_launches(inputs.workload("compressed_128k"), 4096) == 3
+
+
+def test_multi_chunk_prompts_count_every_chunk():
+    """A multi-chunk prompt's step is the whole prompt. prompt_16k: chunks 1-4 fit
+    index_topk (skip path: pool, fill, attention), chunks 5-8 score in one 2048-row
+    tile (pool, score, top-k, attention). two_chunks_4098: the first chunk takes the
+    skip path; the second (2,050 rows: two 2048-row tiles) scores and leaves a
+    2-token remainder."""
+    assert bench.step_launches(inputs.workload("prompt_16k"), 2048) == 4 * 3 + 4 * 4
+    assert bench.step_launches(inputs.workload("two_chunks_4098"), 2048) == 3 + (1 + 1 + 2 * 2 + 1)
+    c = bench.work_counts(inputs.workload("prompt_16k"))
+    # scores only on the full-path chunks 5..8: rows t = 8192..16383, n_vis = floor((t+1)/4)
+    vis = sum((t + 1) // 4 for t in range(8192, 16384))
+    assert c["score_flops"] == 2 * 64 * 128 * vis
+    k = 2048
+    keys = sum(min(128, t + 1) + min(k, (t + 1) // 4) for t in range(16384))
+    assert c["attn_flops"] == 4 * 64 * 512 * keys

@@ -19,7 +19,7 @@ from deepseek_v4_sparse_ratio_gb300 import _binding as B
 from deepseek_v4_sparse_ratio_gb300 import inputs
 from deepseek_v4_sparse_ratio_gb300.runner import DeviceWorkload
 
-from parity import bf16_to_f64, check_attention, check_selection
+from parity import attention_reference, bf16_to_f64, check_attention, check_selection
 
 pytestmark = pytest.mark.gpu
 
@@ -52,9 +52,13 @@ def test_wait_without_arrival_times_out_and_context_survives(dsa):
     torch.cuda.synchronize()
     dw.check_status()
     T = 96
-    res = oracle.prefill_chunk(oracle.PoolState(4), wl.t["raw_ik"], wl.t["raw_kv"], 0,
+    ref_state = oracle.PoolState(4)
+    res = oracle.prefill_chunk(ref_state, wl.t["raw_ik"], wl.t["raw_kv"], 0,
                                wl.t["q_idx"], wl.t["w"].numpy(), wl.t["q"], wl.t["raw_kv"], 0,
                                np.arange(T), wl.index_topk, wl.window, 1.0 / math.sqrt(512))
     check_selection(dw.sel[:T].cpu().numpy(), res["sel"], res["pos"], res["n"], wl.index_topk,
                     res["scores"], res["mag"])
-    check_attention(bf16_to_f64(dw.out[:T]), res["out"])
+    gsel = dw.sel[:T].cpu().numpy()
+    ref = attention_reference(res, gsel, wl.t["q"], wl.t["raw_kv"], 0, ref_state.pooled_kv,
+                              wl.window, 1.0 / math.sqrt(512))
+    check_attention(bf16_to_f64(dw.out[:T]), ref)

@@ -1,15 +1,21 @@
 """dsa_prefill_chunk_host: the whole path from pinned host buffers with the
 copies overlapped on a second stream must give exactly what the device path
 gives (same kernels, the attention only split into row slices), chunk after
-chunk, and leave the PoolingCache in the same state."""
+chunk, and leave the PoolingCache in the same state. Its host outputs are also
+checked against the oracle directly on 32 evenly spaced rows per chunk."""
 import math
 
+import numpy as np
 import pytest
 import torch
+
+import oracle
 
 from deepseek_v4_sparse_ratio_gb300 import _binding as B
 from deepseek_v4_sparse_ratio_gb300 import inputs
 from deepseek_v4_sparse_ratio_gb300.runner import DeviceWorkload
+
+from parity import attention_reference, bf16_to_f64, check_attention, check_selection
 
 pytestmark = pytest.mark.gpu
 
@@ -41,6 +47,8 @@ def test_host_path_equals_device_path(dsa, name, copy_stream):
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     side = torch.cuda.Stream() if copy_stream else None
     scale = 1.0 / math.sqrt(B.DIM)
+    ref_state = (oracle.PoolState.from_prefix(wl.t["prefix_ik"], wl.t["prefix_kv"], wl.off0,
+                                              wl.ratio) if wl.off0 else oracle.PoolState(wl.ratio))
     for c, s, T, off in wl.chunk_bounds():
         dw.run_chunk(c)
         torch.cuda.synchronize()
@@ -60,6 +68,17 @@ def test_host_path_equals_device_path(dsa, name, copy_stream):
         assert torch.equal(out_h.view(torch.int16), dw.out[:T].cpu().view(torch.int16))
         assert (st.n_pooled, st.n_tokens, st.n_rem) == \
             (dw.state.n_pooled, dw.state.n_tokens, dw.state.n_rem)
+        rows = inputs.sample_rows(T, 32)
+        res = oracle.prefill_chunk(ref_state, wl.t["raw_ik"][s:s + T], wl.t["raw_kv"][s:s + T],
+                                   off, wl.t["q_idx"][s:s + T], wl.t["w"][s:s + T].numpy(),
+                                   wl.t["q"][s:s + T], raw_all, raw_base, rows, wl.index_topk, W,
+                                   scale)
+        gsel = sel_h.numpy()[rows]
+        check_selection(gsel, res["sel"], res["pos"], res["n"], wl.index_topk, res["scores"],
+                        res["mag"], ratio=wl.ratio)
+        ref = attention_reference(res, gsel, wl.t["q"][s:s + T][rows], raw_all, raw_base,
+                                  ref_state.pooled_kv, W, scale)
+        check_attention(bf16_to_f64(out_h[rows]), ref)
     n = st.n_pooled
     assert torch.equal(st.pooled_kv[:n], dw.state.pooled_kv[:n])
     assert torch.equal(st.pooled_ik[:n], dw.state.pooled_ik[:n])

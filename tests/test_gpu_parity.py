@@ -16,7 +16,8 @@ from deepseek_v4_sparse_ratio_gb300 import _binding as B
 from deepseek_v4_sparse_ratio_gb300 import inputs
 from deepseek_v4_sparse_ratio_gb300.runner import DeviceWorkload
 
-from parity import bf16_to_f64, check_attention, check_scores, check_selection
+from parity import (attention_reference, bf16_to_f64, check_attention, check_scores,
+                    check_selection)
 
 pytestmark = pytest.mark.gpu
 
@@ -286,11 +287,34 @@ def _oracle_prefix_state(wl):
     return oracle.PoolState(wl.ratio)
 
 
-def run_workload_parity(wl, tile_rows, sample):
+def _scratch_rows(dw, T, n, rows):
+    """GPU scores of chunk-local `rows` still held in the score scratch after a
+    chunk: the scratch holds the chunk's last tile (rows [last0, T)); returns
+    (positions in `rows` of the rows found there, their scores [m, n])."""
+    tile = min(dw.tile_rows, T)
+    last0 = ((T - 1) // tile) * tile
+    stride = (n + 127) // 128 * 128
+    idx = [i for i, r in enumerate(rows) if r >= last0]
+    if not idx:
+        return idx, None
+    local = torch.tensor([rows[i] - last0 for i in idx], device=dw.scratch.device)
+    held = dw.scratch[: (T - last0) * stride].view(T - last0, stride)
+    return idx, held.index_select(0, local)[:, :n].cpu().numpy()
+
+
+def run_workload_parity(wl, tile_rows, sample, stats=None, keep=False):
+    """Every chunk of the workload through dsa_prefill_chunk, compared with the
+    oracle on the chunk-local rows inputs.sample_rows(T, sample) (all rows when
+    sample is 0): selection (tie-band rule), the scores of those rows that the
+    last tile left in the scratch (element-wise), the attention output (against
+    the oracle's attention over the GPU's own selection where the two selections
+    differ inside the tie band), and the pooled cache bit for bit. Returns the
+    GPU selections, and with keep=True also each chunk's (rows, oracle result)."""
     dw = DeviceWorkload(wl, tile_rows=tile_rows)
     ref_state = _oracle_prefix_state(wl)
     raw_all = torch.cat([wl.t["prefix_win"], wl.t["raw_kv"]], 0)
-    sels = []
+    stats = {} if stats is None else stats
+    sels, kept = [], []
     for c, s, T, off in wl.chunk_bounds():
         dw.run_chunk(c)
         torch.cuda.synchronize()
@@ -300,19 +324,31 @@ def run_workload_parity(wl, tile_rows, sample):
                                    off, wl.t["q_idx"][s:s + T], wl.t["w"][s:s + T].numpy(),
                                    wl.t["q"][s:s + T], raw_all, dw.raw_start, rows,
                                    wl.index_topk, wl.window, SCALE)
-        assert dw.state.n_pooled == res["n"] == (off + T) // wl.ratio
+        n = res["n"]
+        assert dw.state.n_pooled == n == (off + T) // wl.ratio
         gsel = dw.sel[:T].cpu().numpy()
         sels.append(gsel)
-        check_selection(gsel[rows], res["sel"], res["pos"], res["n"], wl.index_topk,
-                        res["scores"], res["mag"], ratio=wl.ratio)
-        same = np.all(gsel[rows] == res["sel"], axis=1)
-        check_attention(bf16_to_f64(dw.out[rows]), res["out"], same)
+        check_selection(gsel[rows], res["sel"], res["pos"], n, wl.index_topk,
+                        res["scores"], res["mag"], ratio=wl.ratio, stats=stats)
+        if res["scores"] is not None:
+            idx, gs = _scratch_rows(dw, T, n, rows)
+            if idx:
+                check_scores(gs, res["scores"][idx], res["mag"][idx], stats)
+                stats["score_rows"] = stats.get("score_rows", 0) + len(idx)
+        ref_out = attention_reference(res, gsel[rows], wl.t["q"][s:s + T][rows], raw_all,
+                                      dw.raw_start, ref_state.pooled_kv, wl.window, SCALE)
+        err = check_attention(bf16_to_f64(dw.out[rows]), ref_out)
+        stats["attn_rel_err"] = max(stats.get("attn_rel_err", 0.0), err)
+        stats["attn_rows"] = stats.get("attn_rows", 0) + len(rows)
+        if keep:
+            kept.append((rows, res))
     n = ref_state.n_pooled
     lo = wl.prefix_pooled
     assert np.array_equal(_bits(dw.state.pooled_kv[lo:n]), ref_state.pooled_kv[lo:n])
     assert np.array_equal(_bits(dw.state.pooled_ik[lo:n]), ref_state.pooled_ik[lo:n])
     assert dw.state.n_rem == ref_state.n_rem
-    return sels
+    print(f"\n{wl.name} tile {tile_rows}: {stats}")
+    return (sels, kept) if keep else sels
 
 
 @pytest.mark.parametrize("name", ["zero_prefix_512", "two_chunks_4098", "prompt_16k"])
@@ -328,10 +364,26 @@ def test_workload_parity(dsa, name):
 
 @pytest.mark.parametrize("name", ["ctx_128k", "ctx_1m"])
 def test_long_context_parity_and_tile_invariance(dsa, name):
+    """Full size, the benchmark's launch configuration: sampled rows against the
+    oracle, then the other tile size must give the same selection; the scores of
+    every sampled row held by the last tile of either run are compared element
+    by element (ctx_128k: one 4096-row tile; ctx_1m: rows 3072-4095 of the
+    1024-row tiling, then all sampled rows of the 4096-row tile, which spans
+    2,048 key blocks in the score kernel's segments)."""
     wl = inputs.draw(inputs.workload(name))
-    sels = run_workload_parity(wl, wl.tile_rows[0], wl.sample_rows)
+    stats = {}
+    sels, kept = run_workload_parity(wl, wl.tile_rows[0], wl.sample_rows, stats, keep=True)
     other = wl.tile_rows[1]
     dw = DeviceWorkload(wl, tile_rows=other)
     dw.run_chunk(0)
     torch.cuda.synchronize()
+    dw.check_status()
     assert np.array_equal(dw.sel[:wl.chunks[0]].cpu().numpy(), sels[0]), "tiling changed an index"
+    rows, res = kept[0]
+    idx, gs = _scratch_rows(dw, wl.chunks[0], res["n"], rows)
+    assert idx
+    check_scores(gs, res["scores"][idx], res["mag"][idx], stats)
+    stats["score_rows"] += len(idx)
+    print(f"{name} after tile {other}: {stats}")
+    if name == "ctx_128k":
+        assert stats["score_rows"] == 2 * len(rows)
