@@ -46,20 +46,374 @@ namespace dsa {
 
 namespace {
 
+// ------------------------------------------------------------------ top-k helpers
+//
+// The top-k runs either as CTAs of its own (topk_kernel) or as a group of warps
+// inside the score kernel that selects the rows of the tile before (ping-pong
+// scratch). The helpers below work for a group of NT threads: `tid` is the
+// thread's index in the group (the group starts at a warp boundary) and `sync`
+// is the group's barrier.
+
+constexpr int kBins = 2048;
+constexpr int kCandCap = 2048;
+
+__device__ __forceinline__ uint32_t order_key(float f) {
+    const uint32_t b = __float_as_uint(f);
+    return b ^ ((b & 0x80000000u) ? 0xFFFFFFFFu : 0x80000000u);
+}
+
+struct CtaSync {
+    __device__ __forceinline__ void operator()() const { __syncthreads(); }
+};
+
+// Named barrier kId over kThreads threads.
+template <int kId, int kThreads>
+struct GroupSync {
+    __device__ __forceinline__ void operator()() const {
+        asm volatile("bar.sync %0, %1;" ::"n"(kId), "n"(kThreads) : "memory");
+    }
+};
+
+// Shared memory of one top-k group.
+template <int NT>
+struct TopkShared {
+    uint32_t hist[kBins];
+    uint32_t cand[kCandCap];
+    int32_t cand_j[kCandCap];
+    uint32_t warp_sums[NT / 32 + 1];
+    uint32_t s_bin, s_above, s_cnt;
+    float s_min[NT / 32], s_max[NT / 32];
+    uint32_t w_gt[NT / 32], w_eq[NT / 32];
+};
+
+// Exclusive group-wide prefix sum of a per-thread value; *total gets the sum.
+template <int NT, class Sync>
+__device__ __forceinline__ uint32_t group_excl_scan(uint32_t v, int tid, uint32_t *warp_sums,
+                                                    uint32_t *total, Sync sync) {
+    const int lane = tid & 31, warp = tid >> 5;
+    uint32_t inc = v;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
+        if (lane >= o) inc += y;
+    }
+    if (lane == 31) warp_sums[warp] = inc;
+    sync();
+    if (warp == 0) {
+        uint32_t x = lane < (NT / 32) ? warp_sums[lane] : 0;
+        uint32_t xi = x;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, xi, o);
+            if (lane >= o) xi += y;
+        }
+        if (lane < (NT / 32)) warp_sums[lane] = xi - x;
+        if (lane == (NT / 32) - 1) warp_sums[(NT / 32)] = xi;
+    }
+    sync();
+    const uint32_t r = warp_sums[warp] + inc - v;
+    *total = warp_sums[(NT / 32)];
+    sync();
+    return r;
+}
+
+// After hist[0..nb) is filled: the bin b holding the `need`-th largest element
+// (counting from the top bin down) and how many elements lie in higher bins.
+template <int NT, class Sync>
+__device__ __forceinline__ void find_bin(const uint32_t *hist, int nb, uint32_t need, int tid,
+                                         uint32_t *warp_sums, uint32_t *s_bin, uint32_t *s_above,
+                                         Sync sync) {
+    const int per = nb / NT;
+    const int top = nb - per * tid;  // thread i owns bins [top-per, top)
+    uint32_t mine = 0;
+    for (int b = top - per; b < top; ++b) mine += hist[b];
+    uint32_t tot;
+    uint32_t cum = group_excl_scan<NT>(mine, tid, warp_sums, &tot, sync);
+    for (int b = top - 1; b >= top - per; --b) {
+        const uint32_t c = hist[b];
+        if (cum < need && need <= cum + c) {
+            *s_bin = static_cast<uint32_t>(b);
+            *s_above = cum;
+        }
+        cum += c;
+    }
+    sync();
+}
+
+// Radix select over `count` order keys given by key_at(i): the key of the
+// need-th largest element and how many elements equal to it are kept
+// (11/11/10-bit digits from the top).
+template <int NT, class Sync, typename KeyAt>
+__device__ __forceinline__ void radix_select(KeyAt key_at, int64_t count, uint32_t need, int tid,
+                                             uint32_t *hist, uint32_t *warp_sums, uint32_t *s_bin,
+                                             uint32_t *s_above, uint32_t *thr_out,
+                                             uint32_t *need_out, Sync sync) {
+    uint32_t prefix = 0;
+    for (int pass = 0; pass < 3; ++pass) {
+        const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
+        const int bits = pass == 2 ? 10 : 11;
+        const int nb = 1 << bits;
+        for (int i = tid; i < nb; i += NT) hist[i] = 0;
+        sync();
+        for (int64_t j = tid; j < count; j += NT) {
+            const uint32_t u = key_at(j);
+            if (pass == 0 || (u >> (shift + bits)) == prefix)
+                atomicAdd(&hist[(u >> shift) & (nb - 1)], 1u);
+        }
+        sync();
+        find_bin<NT>(hist, nb, need, tid, warp_sums, s_bin, s_above, sync);
+        prefix = (prefix << bits) | *s_bin;
+        need -= *s_above;
+        sync();
+    }
+    *thr_out = prefix;
+    *need_out = need;
+}
+
+// Top-k of one score row (L visible scores, L > k) by a group of NT threads,
+// with U 16-byte loads in flight per thread in every pass. The same algorithm
+// as topk_kernel: 2048 linear bins between the row's min and max (from the
+// score kernel's segment ranges parked in out[2s], out[2s+1] when nseg > 0),
+// the threshold bin's scores as candidates (ranked against each other, or
+// radix-selected when crowded, or a radix select over the whole row when the
+// bin overflows), then emission of the kept indices in index order. Each warp
+// owns a contiguous segment of whole 128-score pieces; within a piece lane l
+// holds scores 4l..4l+3, and a warp prefix sum orders the emitted indices.
+template <int NT, int U, class Sync>
+__device__ void topk_row_vec(const float *__restrict__ src, int64_t L, int32_t k, int32_t nseg,
+                             int32_t *__restrict__ out, TopkShared<NT> &sh, int tid, Sync sync) {
+    constexpr int NW = NT / 32;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int64_t seg = ((L + NW - 1) / NW + 127) / 128 * 128;
+    const int64_t lo = min(L, seg * warp), hi = min(L, seg * (warp + 1));
+    // every pass: U pieces of 128 scores per warp in flight, visited in index order
+    // (lanes whose 4 scores start at or beyond hi see nothing; within a load, scores
+    // at or beyond hi are masked by the visitor)
+    auto walk = [&](auto &&visit, bool last_pass) {
+        for (int64_t base = lo; base < hi; base += 128 * U) {
+            float4 v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u) {
+                const int64_t j = base + 128 * u + 4 * lane;
+                const float4 *p = reinterpret_cast<const float4 *>(src + j);
+                v[u] = j < hi ? (last_pass ? __ldcs(p) : __ldcg(p))
+                              : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+            }
+#pragma unroll
+            for (int u = 0; u < U; ++u) visit(base + 128 * u + 4 * lane, v[u]);
+        }
+    };
+    auto elem = [](const float4 &v, int e) { return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w; };
+
+    // ---- 1. range of the row
+    float vmin = INFINITY, vmax = -INFINITY;
+    if (nseg > 0) {
+        if (warp == 0)
+            for (int sg = lane; sg < nseg; sg += 32) {
+                vmin = fminf(vmin, __int_as_float(out[2 * sg]));
+                vmax = fmaxf(vmax, __int_as_float(out[2 * sg + 1]));
+            }
+    } else {
+        walk([&](int64_t j, const float4 &v) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (j + e < hi) {
+                    vmin = fminf(vmin, elem(v, e));
+                    vmax = fmaxf(vmax, elem(v, e));
+                }
+        }, false);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+        vmin = fminf(vmin, __shfl_xor_sync(0xFFFFFFFFu, vmin, o));
+        vmax = fmaxf(vmax, __shfl_xor_sync(0xFFFFFFFFu, vmax, o));
+    }
+    if (lane == 0) {
+        sh.s_min[warp] = vmin;
+        sh.s_max[warp] = vmax;
+    }
+    for (int i = tid; i < kBins; i += NT) sh.hist[i] = 0;
+    if (tid == 0) sh.s_cnt = 0;
+    sync();
+    vmin = sh.s_min[0];
+    vmax = sh.s_max[0];
+#pragma unroll
+    for (int w = 1; w < NW; ++w) {
+        vmin = fminf(vmin, sh.s_min[w]);
+        vmax = fmaxf(vmax, sh.s_max[w]);
+    }
+
+    uint32_t thr, need_eq;
+    bool counted = false;  // w_gt / w_eq already hold the per-segment counts
+    if (vmin == vmax) {
+        // every visible score is equal: the k lowest indices
+        thr = order_key(vmax);
+        need_eq = static_cast<uint32_t>(k);
+    } else {
+        // ---- 2. linear bins between min and max (monotone: every element of a higher
+        // bin is >= every element of a lower bin)
+        const float scale = static_cast<float>(kBins) / (vmax - vmin);
+        auto bin_of = [&](float v) { return min(kBins - 1, static_cast<int>((v - vmin) * scale)); };
+        walk([&](int64_t j, const float4 &v) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (j + e < hi) atomicAdd(&sh.hist[bin_of(elem(v, e))], 1u);
+        }, false);
+        sync();
+        find_bin<NT>(sh.hist, kBins, static_cast<uint32_t>(k), tid, sh.warp_sums, &sh.s_bin,
+                     &sh.s_above, sync);
+        const int bstar = static_cast<int>(sh.s_bin);
+        const uint32_t need = static_cast<uint32_t>(k) - sh.s_above;
+        // ---- 3. the threshold bin's elements are the candidates; each segment's
+        // elements above that bin are counted on the way
+        uint32_t above = 0;
+        walk([&](int64_t j, const float4 &v) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (j + e < hi) {
+                    const int b = bin_of(elem(v, e));
+                    above += b > bstar;
+                    if (b == bstar) {
+                        const uint32_t c = atomicAdd(&sh.s_cnt, 1u);
+                        if (c < kCandCap) {
+                            sh.cand[c] = order_key(elem(v, e));
+                            sh.cand_j[c] = static_cast<int32_t>(j + e);
+                        }
+                    }
+                }
+        }, false);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) above += __shfl_xor_sync(0xFFFFFFFFu, above, o);
+        if (lane == 0) {
+            sh.w_gt[warp] = above;
+            sh.w_eq[warp] = 0;
+        }
+        sync();
+        const uint32_t cnt = sh.s_cnt;
+        if (cnt <= NT) {
+            // few candidates: each thread ranks one against all of them; the need-th
+            // largest has fewer than `need` strictly larger keys and at least `need`
+            // larger-or-equal ones
+            if (static_cast<uint32_t>(tid) < cnt) {
+                const uint32_t u = sh.cand[tid];
+                uint32_t gt = 0, ge = 0;
+                for (uint32_t c = 0; c < cnt; ++c) {
+                    const uint32_t w = sh.cand[c];
+                    gt += w > u;
+                    ge += w >= u;
+                }
+                if (gt < need && need <= ge) {  // every thread holding that key agrees
+                    sh.s_bin = u;
+                    sh.s_above = need - gt;
+                }
+            }
+            sync();
+            thr = sh.s_bin;
+            need_eq = sh.s_above;
+        } else if (cnt <= kCandCap) {
+            radix_select<NT>([&](int64_t c) { return sh.cand[c]; }, cnt, need, tid, sh.hist,
+                             sh.warp_sums, &sh.s_bin, &sh.s_above, &thr, &need_eq, sync);
+        }
+        if (cnt <= kCandCap) {
+            // candidates above / equal to the threshold, by segment
+            for (uint32_t c = tid; c < cnt; c += NT) {
+                const int w = static_cast<int>(sh.cand_j[c] / seg);
+                if (sh.cand[c] > thr) atomicAdd(&sh.w_gt[w], 1u);
+                else if (sh.cand[c] == thr) atomicAdd(&sh.w_eq[w], 1u);
+            }
+            sync();
+            counted = true;
+        } else {
+            radix_select<NT>([&](int64_t j) { return order_key(src[j]); }, L,
+                             static_cast<uint32_t>(k), tid, sh.hist, sh.warp_sums, &sh.s_bin,
+                             &sh.s_above, &thr, &need_eq, sync);
+        }
+    }
+
+    if (!counted) {
+        uint32_t ngt = 0, neq = 0;
+        walk([&](int64_t j, const float4 &v) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (j + e < hi) {
+                    const uint32_t u = order_key(elem(v, e));
+                    ngt += u > thr;
+                    neq += u == thr;
+                }
+        }, false);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            ngt += __shfl_xor_sync(0xFFFFFFFFu, ngt, o);
+            neq += __shfl_xor_sync(0xFFFFFFFFu, neq, o);
+        }
+        if (lane == 0) {
+            sh.w_gt[warp] = ngt;
+            sh.w_eq[warp] = neq;
+        }
+        sync();
+    }
+    // ---- 4. emit kept indices ascending: kept element j goes to
+    // (#above-threshold before j) + min(#equal before j, need_eq)
+    uint32_t base_gt = 0, base_eq = 0;
+    for (int w = 0; w < warp; ++w) {
+        base_gt += sh.w_gt[w];
+        base_eq += sh.w_eq[w];
+    }
+    walk([&](int64_t j, const float4 &v) {
+        uint32_t gm = 0, em = 0;
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if (j + e < hi) {
+                const uint32_t u = order_key(elem(v, e));
+                gm |= static_cast<uint32_t>(u > thr) << e;
+                em |= static_cast<uint32_t>(u == thr) << e;
+            }
+        // lane-order prefix of (above, equal) counts, packed in 16-bit halves (at
+        // most 128 of each per piece)
+        const uint32_t mine = static_cast<uint32_t>(__popc(gm)) |
+                              (static_cast<uint32_t>(__popc(em)) << 16);
+        uint32_t incl = mine;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, incl, o);
+            if (lane >= o) incl += y;
+        }
+        const uint32_t excl = incl - mine;
+        const uint32_t gb = base_gt + (excl & 0xFFFFu), eb = base_eq + (excl >> 16);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const uint32_t below = (1u << e) - 1u;
+            const uint32_t ng = gb + __popc(gm & below), ne = eb + __popc(em & below);
+            if ((gm >> e) & 1u) out[ng + min(ne, need_eq)] = static_cast<int32_t>(j + e);
+            else if (((em >> e) & 1u) && ne < need_eq) out[ng + ne] = static_cast<int32_t>(j + e);
+        }
+        const uint32_t tot = __shfl_sync(0xFFFFFFFFu, incl, 31);
+        base_gt += tot & 0xFFFFu;
+        base_eq += tot >> 16;
+    }, true);
+}
+
 // ------------------------------------------------------------------ score kernel
 
 constexpr int kTok = 8;            // query rows per work unit
 constexpr int kStages = 2;         // key-block ring depth
 constexpr int kEpiWarps = 16;      // one 4-row x 32-lane slice of a TMEM half each
-constexpr int kScoreThreads = 32 * (2 + kEpiWarps);  // warp 0 TMA, warp 1 MMA, 2-17 epilogue
+// warp 0 TMA, warp 1 MMA, warps 2-3 the top-k of the previous tile, 4-19 epilogue
+constexpr int kTopkWarp0 = 2;
+constexpr int kTopkGroup = 64;     // threads of the in-kernel top-k group
+constexpr int kEpiWarp0 = 4;
+constexpr int kScoreThreads = 32 * (kEpiWarp0 + kEpiWarps);
 constexpr uint32_t kBBytes = 2 * 2 * 256 * 128;  // [half][k-chunk][256 rows][128 B]
 constexpr uint32_t kAStage = 2 * 128 * 128;      // [k-chunk][128 rows][128 B]
 constexpr uint32_t kOffB = 0;
 constexpr uint32_t kOffA = kOffB + kBBytes;
 constexpr uint32_t kOffW = kOffA + kStages * kAStage;
 constexpr uint32_t kOffRng = kOffW + kTok * kHI * 4;  // [16 epilogue warps][4] partial ranges
-constexpr uint32_t kOffBar = kOffRng + kEpiWarps * 4 * 4;
+constexpr uint32_t kOffTopk = kOffRng + kEpiWarps * 4 * 4;
+constexpr uint32_t kOffBar =
+    kOffTopk + (static_cast<uint32_t>(sizeof(TopkShared<kTopkGroup>)) + 15u) / 16u * 16u;
 constexpr uint32_t kScoreSmem = kOffBar + 256 + 1024;  // + slack for 1024-B alignment
+static_assert(kScoreSmem <= 232448, "over the shared memory of one CTA");
 
 struct ScoreParams {
     const float *w;   // [chunk, 64]
@@ -76,6 +430,14 @@ struct ScoreParams {
     int32_t *rng;     // selection rows [chunk, k] used as range scratch, or null
     int32_t k;        // selection row length
     int32_t *status;
+    // the previous tile, whose top-k the kernel's top-k warps run (ping-pong scratch):
+    // its scores (the other half of the scratch), first chunk row, rows (0: none) and
+    // the segment count of its parked row ranges (0: none)
+    const float *prev_scores;
+    int64_t prev_r0;
+    int prev_R;
+    int prev_nseg;
+    int32_t *sel;     // selection [chunk, k]
 };
 
 struct Unit {
@@ -243,10 +605,29 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         // every MMA issued above must have finished before TMEM is released
         mma_commit(drain);
         drain_wait(drain, 0);
-    } else if (warp >= 2) {
+    } else if (warp >= kTopkWarp0 && warp < kEpiWarp0) {
+        // ---------------- top-k of the previous tile's rows (its scores sit in the other
+        // half of the scratch), last rows first, spread over the CTAs
+        TopkShared<kTopkGroup> &sh = *reinterpret_cast<TopkShared<kTopkGroup> *>(smem + kOffTopk);
+        const int tid = threadIdx.x - 32 * kTopkWarp0;
+        for (int it = blockIdx.x; it < p.prev_R; it += gridDim.x) {
+            const int row = p.prev_R - 1 - it;
+            const int64_t t = p.offset + p.prev_r0 + row;
+            const int64_t L = min(p.n, (t + 1) / p.ratio);
+            int32_t *out = p.sel + (p.prev_r0 + row) * static_cast<int64_t>(p.k);
+            if (L <= p.k) {
+                for (int i = tid; i < p.k; i += kTopkGroup) out[i] = i < L ? i : -1;
+                continue;
+            }
+            topk_row_vec<kTopkGroup, 8>(p.prev_scores + static_cast<int64_t>(row) * p.stride, L,
+                                        p.k, p.prev_nseg, out, sh, tid,
+                                        GroupSync<2, kTopkGroup>{});
+            GroupSync<2, kTopkGroup>{}();  // the shared arrays are reused by the next row
+        }
+    } else if (warp >= kEpiWarp0) {
         // ---------------- epilogue: 16 warps; warp reads TMEM sub-partition sp = warp % 4
         // (pooled rows j = 32sp .. 32sp+31 of the block) for token tl of each 4-token half
-        const int ew = warp - 2;
+        const int ew = warp - kEpiWarp0;
         const int sp = warp & 3;
         const int tl = ew >> 2;
         const uint32_t lane_addr = tmem + (static_cast<uint32_t>(sp * 32) << 16);
@@ -377,96 +758,6 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 // enough to fill the GPU and the rows are short, else 1024
 constexpr int kTopkThreads = 256;
 constexpr int kTopkThreadsFew = 1024;
-constexpr int kBins = 2048;
-constexpr int kCandCap = 2048;
-
-__device__ __forceinline__ uint32_t order_key(float f) {
-    const uint32_t b = __float_as_uint(f);
-    return b ^ ((b & 0x80000000u) ? 0xFFFFFFFFu : 0x80000000u);
-}
-
-// Exclusive block-wide prefix sum of a per-thread value; *total gets the sum.
-template <int NT>
-__device__ __forceinline__ uint32_t block_excl_scan(uint32_t v, uint32_t *warp_sums,
-                                                    uint32_t *total) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    uint32_t inc = v;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, inc, o);
-        if (lane >= o) inc += y;
-    }
-    if (lane == 31) warp_sums[warp] = inc;
-    __syncthreads();
-    if (warp == 0) {
-        uint32_t x = lane < (NT / 32) ? warp_sums[lane] : 0;
-        uint32_t xi = x;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const uint32_t y = __shfl_up_sync(0xFFFFFFFFu, xi, o);
-            if (lane >= o) xi += y;
-        }
-        if (lane < (NT / 32)) warp_sums[lane] = xi - x;
-        if (lane == (NT / 32) - 1) warp_sums[(NT / 32)] = xi;
-    }
-    __syncthreads();
-    const uint32_t r = warp_sums[warp] + inc - v;
-    *total = warp_sums[(NT / 32)];
-    __syncthreads();
-    return r;
-}
-
-// After hist[0..nb) is filled: the bin b holding the `need`-th largest element
-// (counting from the top bin down) and how many elements lie in higher bins.
-template <int NT>
-__device__ __forceinline__ void find_bin(const uint32_t *hist, int nb, uint32_t need,
-                                         uint32_t *warp_sums, uint32_t *s_bin, uint32_t *s_above) {
-    const int per = nb / NT;
-    const int top = nb - per * threadIdx.x;  // thread i owns bins [top-per, top)
-    uint32_t mine = 0;
-    for (int b = top - per; b < top; ++b) mine += hist[b];
-    uint32_t tot;
-    uint32_t cum = block_excl_scan<NT>(mine, warp_sums, &tot);
-    for (int b = top - 1; b >= top - per; --b) {
-        const uint32_t c = hist[b];
-        if (cum < need && need <= cum + c) {
-            *s_bin = static_cast<uint32_t>(b);
-            *s_above = cum;
-        }
-        cum += c;
-    }
-    __syncthreads();
-}
-
-// Radix select over `count` order keys given by key_at(i): the key of the
-// need-th largest element and how many elements equal to it are kept
-// (11/11/10-bit digits from the top).
-template <int NT, typename KeyAt>
-__device__ __forceinline__ void radix_select(KeyAt key_at, int64_t count, uint32_t need,
-                                             uint32_t *hist, uint32_t *warp_sums, uint32_t *s_bin,
-                                             uint32_t *s_above, uint32_t *thr_out,
-                                             uint32_t *need_out) {
-    uint32_t prefix = 0;
-    for (int pass = 0; pass < 3; ++pass) {
-        const int shift = pass == 0 ? 21 : (pass == 1 ? 10 : 0);
-        const int bits = pass == 2 ? 10 : 11;
-        const int nb = 1 << bits;
-        for (int i = threadIdx.x; i < nb; i += NT) hist[i] = 0;
-        __syncthreads();
-        for (int64_t j = threadIdx.x; j < count; j += NT) {
-            const uint32_t u = key_at(j);
-            if (pass == 0 || (u >> (shift + bits)) == prefix)
-                atomicAdd(&hist[(u >> shift) & (nb - 1)], 1u);
-        }
-        __syncthreads();
-        find_bin<NT>(hist, nb, need, warp_sums, s_bin, s_above);
-        prefix = (prefix << bits) | *s_bin;
-        need -= *s_above;
-        __syncthreads();
-    }
-    *thr_out = prefix;
-    *need_out = need;
-}
 
 // One CTA per query row; every pass walks the row in per-warp contiguous
 // segments (coalesced, and the last pass must emit in index order). Rows are
@@ -546,7 +837,8 @@ __global__ void __launch_bounds__(NT)
         auto bin_of = [&](float v) { return min(kBins - 1, static_cast<int>((v - vmin) * scale)); };
         for (int64_t j = lo + lane; j < hi; j += 32) atomicAdd(&hist[bin_of(src[j])], 1u);
         __syncthreads();
-        find_bin<NT>(hist, kBins, static_cast<uint32_t>(k), warp_sums, &s_bin, &s_above);
+        find_bin<NT>(hist, kBins, static_cast<uint32_t>(k), threadIdx.x, warp_sums, &s_bin,
+                     &s_above, CtaSync{});
         const int bstar = static_cast<int>(s_bin);
         const uint32_t need = static_cast<uint32_t>(k) - s_above;
         // ---- 3. the threshold bin's elements are the candidates; count each
@@ -594,8 +886,8 @@ __global__ void __launch_bounds__(NT)
             thr = s_bin;
             need_eq = s_above;
         } else if (cnt <= kCandCap) {
-            radix_select<NT>([&](int64_t c) { return cand[c]; }, cnt, need, hist, warp_sums, &s_bin,
-                         &s_above, &thr, &need_eq);
+            radix_select<NT>([&](int64_t c) { return cand[c]; }, cnt, need, threadIdx.x, hist,
+                             warp_sums, &s_bin, &s_above, &thr, &need_eq, CtaSync{});
         }
         if (cnt <= kCandCap) {
             // candidates above / equal to the threshold, by segment
@@ -607,8 +899,9 @@ __global__ void __launch_bounds__(NT)
             __syncthreads();
             counted = true;
         } else {
-            radix_select<NT>([&](int64_t j) { return order_key(src[j]); }, L, static_cast<uint32_t>(k),
-                         hist, warp_sums, &s_bin, &s_above, &thr, &need_eq);
+            radix_select<NT>([&](int64_t j) { return order_key(src[j]); }, L,
+                             static_cast<uint32_t>(k), threadIdx.x, hist, warp_sums, &s_bin,
+                             &s_above, &thr, &need_eq, CtaSync{});
         }
     }
 
@@ -649,14 +942,23 @@ __global__ void __launch_bounds__(NT)
 }
 
 // Selection without scoring: sel[i, c] = c if c < n_vis(t) else -1 (n = 0: all -1).
-__global__ void fill_selection_kernel(int32_t *sel, int64_t rows, int32_t k, int64_t offset,
-                                      int64_t n, int32_t ratio) {
-    const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (idx >= rows * k) return;
-    const int64_t i = idx / k;
-    const int32_t c = static_cast<int32_t>(idx % k);
+// One CTA per row; 16-byte stores of four entries when k is a multiple of 4.
+__global__ void __launch_bounds__(256) fill_selection_kernel(int32_t *sel, int32_t k,
+                                                             int64_t offset, int64_t n,
+                                                             int32_t ratio) {
+    const int64_t i = blockIdx.x;
     const int64_t nv = min(n, (offset + i + 1) / ratio);
-    sel[idx] = c < nv ? c : -1;
+    int32_t *row = sel + i * k;
+    if ((k & 3) == 0) {
+        int4 *row4 = reinterpret_cast<int4 *>(row);
+        for (int c4 = threadIdx.x; c4 < (k >> 2); c4 += blockDim.x) {
+            const int c = 4 * c4;
+            row4[c4] = make_int4(c < nv ? c : -1, c + 1 < nv ? c + 1 : -1,
+                                 c + 2 < nv ? c + 2 : -1, c + 3 < nv ? c + 3 : -1);
+        }
+    } else {
+        for (int c = threadIdx.x; c < k; c += blockDim.x) row[c] = c < nv ? c : -1;
+    }
 }
 
 int choose_segments(int groups, int NB, int sms) {
@@ -680,15 +982,19 @@ int choose_segments(int groups, int NB, int sms) {
 
 int launch_fill_selection(int32_t *sel, int64_t rows, int32_t k, int64_t offset, int64_t n,
                           int32_t ratio, cudaStream_t s) {
-    const int64_t total = rows * k;
-    fill_selection_kernel<<<static_cast<unsigned>((total + 255) / 256), 256, 0, s>>>(
-        sel, rows, k, offset, n, ratio);
+    const int threads = k >= 1024 ? 256 : (k >= 256 ? 128 : 64);
+    fill_selection_kernel<<<static_cast<unsigned>(rows), threads, 0, s>>>(sel, k, offset, n,
+                                                                           ratio);
     return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
+// Scores of tile rows [r0, r0 + R) into `scores`; with prev_R > 0 the kernel's
+// top-k warps also select the rows [prev_r0, prev_r0 + prev_R) of the previous
+// tile from prev_scores (prev_nseg: that tile's parked range count).
 int launch_score_tile(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const float *w, int64_t n,
                       int64_t offset, int32_t ratio, int64_t r0, int64_t R, float *scores,
                       int64_t stride, int32_t *sel, int32_t k, int *nseg_rng, int32_t *status,
+                      const float *prev_scores, int64_t prev_r0, int64_t prev_R, int prev_nseg,
                       cudaStream_t s) {
     const int sms = std::max(1, sm_count());
     ScoreParams p;
@@ -710,6 +1016,11 @@ int launch_score_tile(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const fl
     p.k = k;
     if (nseg_rng) *nseg_rng = rng ? p.nseg : 0;
     p.status = status;
+    p.prev_scores = prev_scores;
+    p.prev_r0 = prev_r0;
+    p.prev_R = static_cast<int>(prev_R);
+    p.prev_nseg = prev_nseg;
+    p.sel = sel;
     const int grid = std::min(p.n_units, sms);
     score_kernel<<<grid, kScoreThreads, kScoreSmem, s>>>(tm_q, tm_k, p);
     return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
@@ -788,20 +1099,48 @@ int prepare_score_topk(const void *q_idx, const void *pooled_ik, int64_t n, int6
 
 int enqueue_score_topk(const ScoreTopkPlan &plan, const float *w, int64_t n, int64_t chunk,
                        int64_t offset, int32_t ratio, int32_t k, int64_t tile_rows,
-                       void *scratch, int32_t *sel, int32_t *status, cudaStream_t s) {
+                       void *scratch, size_t scratch_bytes, int32_t *sel, int32_t *status,
+                       cudaStream_t s) {
     if (!plan.full) return launch_fill_selection(sel, chunk, k, offset, n, ratio, s);
     const int64_t stride = score_stride(n);
     float *scores = static_cast<float *>(scratch);
-    for (int64_t r0 = 0; r0 < chunk; r0 += tile_rows) {
-        const int64_t R = std::min(tile_rows, chunk - r0);
-        int nseg_rng = 0;
-        int rc = launch_score_tile(plan.tm_q, plan.tm_k, w, n, offset, ratio, r0, R, scores,
-                                   stride, sel, k, &nseg_rng, status, s);
-        if (rc != DSA_OK) return rc;
-        rc = launch_topk_tile(scores, stride, n, offset, ratio, r0, R, k, nseg_rng, sel, status, s);
-        if (rc != DSA_OK) return rc;
+    const int64_t tile = std::min(tile_rows, chunk);
+    // Two tile buffers in the scratch and more than one tile: ping-pong. The score
+    // kernel of tile i writes one buffer while its top-k warps select tile i-1 from
+    // the other; only the last tile's top-k runs on its own.
+    const bool pingpong =
+        chunk > tile && scratch_bytes / 2 >= dsa_score_scratch_bytes(tile, n);
+    if (!pingpong) {
+        for (int64_t r0 = 0; r0 < chunk; r0 += tile) {
+            const int64_t R = std::min(tile, chunk - r0);
+            int nseg_rng = 0;
+            int rc = launch_score_tile(plan.tm_q, plan.tm_k, w, n, offset, ratio, r0, R, scores,
+                                       stride, sel, k, &nseg_rng, status, nullptr, 0, 0, 0, s);
+            if (rc != DSA_OK) return rc;
+            rc = launch_topk_tile(scores, stride, n, offset, ratio, r0, R, k, nseg_rng, sel,
+                                  status, s);
+            if (rc != DSA_OK) return rc;
+        }
+        return DSA_OK;
     }
-    return DSA_OK;
+    const int64_t half = tile * stride;  // floats of one tile buffer
+    int64_t prev_r0 = 0, prev_R = 0;
+    int prev_nseg = 0, i = 0;
+    for (int64_t r0 = 0; r0 < chunk; r0 += tile, ++i) {
+        const int64_t R = std::min(tile, chunk - r0);
+        float *buf = scores + (i & 1) * half;
+        const float *prev = scores + ((i + 1) & 1) * half;
+        int nseg_rng = 0;
+        int rc = launch_score_tile(plan.tm_q, plan.tm_k, w, n, offset, ratio, r0, R, buf, stride,
+                                   sel, k, &nseg_rng, status, prev, prev_r0, prev_R, prev_nseg,
+                                   s);
+        if (rc != DSA_OK) return rc;
+        prev_r0 = r0;
+        prev_R = R;
+        prev_nseg = nseg_rng;
+    }
+    return launch_topk_tile(scores + ((i + 1) & 1) * half, stride, n, offset, ratio, prev_r0,
+                            prev_R, k, prev_nseg, sel, status, s);
 }
 
 }  // namespace dsa
@@ -825,7 +1164,8 @@ extern "C" int dsa_index_score_topk(const void *q_idx, const float *w, const voi
     rc = prepare_score_topk(q_idx, pooled_ik, n_pooled, chunk, index_topk, &plan);
     if (rc != DSA_OK) return rc;
     return enqueue_score_topk(plan, w, n_pooled, chunk, offset, ratio, index_topk, tile_rows,
-                              scratch, sel, dev_status, static_cast<cudaStream_t>(stream));
+                              scratch, scratch_bytes, sel, dev_status,
+                              static_cast<cudaStream_t>(stream));
 }
 
 // ------------------------------------------------------------------ no-allocation variant
@@ -915,6 +1255,9 @@ extern "C" int dsa_index_score_topk_noalloc(const void *q_idx, const float *w,
     ScoreTopkPlan plan;
     rc = prepare_score_topk(q_idx, pooled_ik, n_pooled, chunk, index_topk, &plan);
     if (rc != DSA_OK) return rc;
+    // one tile buffer: the tiles run one after another, as with a one-tile caller scratch
+    const size_t one_tile = dsa_score_scratch_bytes(std::min(tile_rows, chunk), n_pooled);
     return enqueue_score_topk(plan, w, n_pooled, chunk, offset, ratio, index_topk, tile_rows,
-                              scratch, sel, dev_status, static_cast<cudaStream_t>(stream));
+                              scratch, one_tile, sel, dev_status,
+                              static_cast<cudaStream_t>(stream));
 }

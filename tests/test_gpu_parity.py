@@ -189,6 +189,82 @@ def test_topk_heavy_ties_on_every_selection_path(dsa, L, m, k, T):
     assert np.array_equal(sel.cpu().numpy(), oracle.topk(gpu_s, pos, n, 4, k))
 
 
+@pytest.mark.parametrize("off,T,k,tile", [(4096, 1000, 256, 333), (20000, 700, 512, 64),
+                                          (8188, 37, 100, 16), (280000, 320, 2048, 100),
+                                          (4096, 1000, 256, 999)])
+def test_pingpong_tiles_match_one_buffer_and_oracle(dsa, off, T, k, tile):
+    """A scratch of two tiles: the score kernel of each tile runs the top-k of the
+    tile before in its own warps (16-byte loads, a 64-thread group), and the last
+    tile's top-k runs alone. The selection must equal the one-buffer run's bit for
+    bit and pass the oracle on every row; the last tile's scores sit in its half
+    of the scratch and are compared element by element."""
+    q_idx, w, pik, n = _score_case(off + T + tile, off, T, k)
+    args = [t.cuda() for t in (q_idx, w, pik)]
+    one = B.dsa_score_scratch_bytes(tile, n)
+    sels = []
+    for buffers in (1, 2):
+        sel = torch.full((T, k), 7, dtype=torch.int32, device="cuda")
+        scratch = torch.empty(buffers * one // 4, dtype=torch.float32, device="cuda")
+        status = torch.zeros(1, dtype=torch.int32, device="cuda")
+        B.dsa_index_score_topk(*args, n, T, off, 4, k, tile, scratch, sel, status)
+        torch.cuda.synchronize()
+        assert status.item() == 0
+        sels.append(sel.cpu())
+    assert torch.equal(sels[0], sels[1])
+    pos = off + np.arange(T)
+    ref_s, mag = oracle.index_scores(q_idx, w.numpy(), pos, pik, n)
+    ref_sel = oracle.topk(ref_s, pos, n, 4, k)
+    check_selection(sels[1].numpy(), ref_sel, pos, n, k, ref_s, mag)
+    # the last tile (index ntiles-1) was written to half (ntiles-1) % 2
+    stride = (n + 127) // 128 * 128
+    ntiles = (T + tile - 1) // tile
+    last0 = (ntiles - 1) * tile
+    half = ((ntiles - 1) % 2) * tile * stride
+    gs = scratch[half: half + (T - last0) * stride].view(T - last0, stride)[:, :n].cpu().numpy()
+    check_scores(gs, ref_s[last0:], mag[last0:])
+
+
+@pytest.mark.parametrize("L,m,k,T", [(4000, 30, 64, 320), (4000, 600, 300, 320),
+                                     (4000, 100, 3000, 320), (70000, 100, 64, 320),
+                                     (70000, 3000, 2048, 96)])
+def test_pingpong_topk_heavy_ties(dsa, L, m, k, T):
+    """The heavy-tie rows of test_topk_heavy_ties_on_every_selection_path through the
+    ping-pong path (tiles of T/4 rows, two tile buffers): the in-kernel top-k group
+    ranks up to 64 candidates against each other, radix-selects a crowded bin, or
+    radix-selects the whole row when the bin overflows. Checked against the oracle's
+    top-k of the GPU's own scores, exactly."""
+    g = torch.Generator().manual_seed(L + m + k + 1)
+    off = 4 * L
+    n = (off + T) // 4
+    v = torch.randn(128, generator=g)
+    q_idx = v.expand(T, 64, 128).to(torch.bfloat16).contiguous()
+    w = torch.rand(T, 64, generator=g) * 0.125 + 0.01
+    pik = torch.randn(n, 128, generator=g)
+    dup = torch.randperm(L, generator=g)[:m]
+    pik[dup] = 8.0 * v / v.norm() * math.sqrt(128)
+    pik = pik.to(torch.bfloat16)
+    tile = T // 4
+    sel = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    one = B.dsa_score_scratch_bytes(tile, n)
+    scratch = torch.empty(2 * one // 4, dtype=torch.float32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.dsa_index_score_topk(q_idx.cuda(), w.cuda(), pik.cuda(), n, T, off, 4, k, tile, scratch,
+                           sel, status)
+    # the scores of every row, for the exact replay: a one-tile-per-row-set rerun
+    # would change nothing, so recompute them in one buffer per tile
+    full = torch.empty(B.dsa_score_scratch_bytes(T, n) // 4, dtype=torch.float32, device="cuda")
+    sel1 = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    B.dsa_index_score_topk(q_idx.cuda(), w.cuda(), pik.cuda(), n, T, off, 4, k, T, full, sel1,
+                           status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    stride = (n + 127) // 128 * 128
+    gpu_s = full[: T * stride].view(T, stride)[:, :n].cpu().numpy()
+    pos = off + np.arange(T)
+    assert np.array_equal(sel.cpu().numpy(), oracle.topk(gpu_s, pos, n, 4, k))
+    assert torch.equal(sel, sel1)
+
+
 @pytest.mark.parametrize("tiles", [(1, 7, 64, 333), (512, 1000)])
 def test_tile_size_changes_no_index(dsa, tiles):
     off, T, k = 4096, 1000, 256
