@@ -80,16 +80,14 @@ def work_counts(wl):
             "topk_bytes": topk_bytes, "pool_bytes": pool_bytes}
 
 
-def score_scratch_bytes(wl, tile, buffers=1):
-    """Peak score-scratch bytes of the workload: the tile buffers (one, or two when the
-    tiles ping-pong) of the largest full-path chunk."""
+def score_scratch_bytes(wl, tile):
+    """Peak score-scratch bytes of the workload: one tile of the largest full-path chunk."""
     from deepseek_v4_sparse_ratio_gb300 import _binding as B
     peak = 0
     for _, _, T, off in wl.chunk_bounds():
         n = (off + T) // wl.ratio
         if n > wl.index_topk:
-            used = buffers if T > tile else 1
-            peak = max(peak, used * B.dsa_score_scratch_bytes(min(tile, T), n))
+            peak = max(peak, B.dsa_score_scratch_bytes(min(tile, T), n))
     return peak
 
 
@@ -312,13 +310,12 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
-def run_config(wl, name, tile, world, buffers=None):
+def run_config(wl, name, tile, world):
     """The `config` object of both arms' JSON lines."""
     T = wl.chunks[0]
     return {"workload": WORKLOAD_DESC if name == WORKLOAD else name,
             "name": wl.name, "chunk": T, "context": wl.end, "ratio": wl.ratio,
             "index_topk": wl.index_topk, "tile_rows": tile,
-            "tile_buffers": buffers or wl.tile_buffers,
             "pooled_rows": (wl.off0 + T) // wl.ratio,
             "l2": "flushed between steps (512 MiB write, outside the step events)",
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU"}
@@ -413,8 +410,7 @@ def measure_config(name, tile, dev, stream, flush, steps, peak_tf, clock_index):
     from deepseek_v4_sparse_ratio_gb300.runner import DeviceWorkload
     wl = inputs.draw(inputs.workload(name))
     tile = tile or wl.tile_rows[0]
-    buffers = wl.tile_buffers
-    dw = DeviceWorkload(wl, tile_rows=tile, device=dev, tile_buffers=buffers)
+    dw = DeviceWorkload(wl, tile_rows=tile, device=dev)
     snap = dw.state.snapshot()
     step_ms, clocks, _ = time_steps(dw, wl, snap, flush, stream, steps, 3, clock_index)
     ms = statistics.mean(step_ms)
@@ -423,12 +419,11 @@ def measure_config(name, tile, dev, stream, flush, steps, peak_tf, clock_index):
     attn_tf, st_tf = fractions(counts, comp, peak_tf)
     out = {"ms_per_step": ms, "value": wl.total / (ms * 1e-3), "unit": UNIT,
            "tokens_per_step": wl.total, "chunks": list(wl.chunks), "context": wl.end,
-           "index_topk": wl.index_topk, "tile_rows": tile, "tile_buffers": buffers,
-           "steps": steps, "warmup": 3,
+           "index_topk": wl.index_topk, "tile_rows": tile, "steps": steps, "warmup": 3,
            "components_ms": comp, "attention_frac": attn_tf / peak_tf,
            "score_topk_frac": st_tf / peak_tf if st_tf else None,
            "score_flops": counts["score_flops"], "attn_flops": counts["attn_flops"],
-           "score_scratch_bytes": score_scratch_bytes(wl, tile, buffers), "clocks": clocks,
+           "score_scratch_bytes": score_scratch_bytes(wl, tile), "clocks": clocks,
            "launches_per_step": step_launches(wl, tile)}
     del dw
     torch.cuda.empty_cache()
@@ -443,8 +438,6 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--workload", default=WORKLOAD)
     ap.add_argument("--tile-rows", type=int, default=0)
-    ap.add_argument("--tile-buffers", type=int, default=0,
-                    help="score-scratch tile buffers (2: ping-pong tiles); 0 = the workload's")
     ap.add_argument("--no-cpu", action="store_true", help="skip the oracle CPU baseline")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the other workloads")
@@ -470,8 +463,7 @@ def main():
     inputs.draw(wl)
     T = wl.total
     tile = args.tile_rows or wl.tile_rows[0]
-    buffers = args.tile_buffers or wl.tile_buffers
-    dw = DeviceWorkload(wl, tile_rows=tile, device=dev, tile_buffers=buffers)
+    dw = DeviceWorkload(wl, tile_rows=tile, device=dev)
     stream = torch.cuda.current_stream(dev)
     flush = torch.empty(512 * 2 ** 20 // 4, dtype=torch.float32, device=dev)
     snap = dw.state.snapshot()
@@ -500,7 +492,7 @@ def main():
                 "w": pin(wl.t["w"]), "q": pin(wl.t["q"])}
         out_h = torch.empty(dw.out.shape, dtype=dw.out.dtype).pin_memory()
         sel_h = torch.empty(dw.sel.shape, dtype=dw.sel.dtype).pin_memory()
-        ws = B.PrefillWorkspace(T, k, raw_h.shape[0], n, tile, dev, tile_buffers=buffers)
+        ws = B.PrefillWorkspace(T, k, raw_h.shape[0], n, tile, dev)
         side = torch.cuda.Stream(dev)
         h2d = raw_h.numel() * 2 + sum(t.numel() * t.element_size() for t in host.values())
         d2h = out_h.numel() * out_h.element_size() + sel_h.numel() * sel_h.element_size()
@@ -559,7 +551,7 @@ def main():
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": ms, "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": run_config(wl, args.workload, tile, world, buffers),
+        "config": run_config(wl, args.workload, tile, world),
         # the dominant kernel of the step (about half of its time): window + selected
         # attention, one attn_kernel launch per dsa_window_sparse_attn call
         "roofline": {"kernel": "attn_kernel (dsa_window_sparse_attn)", "bound": "tensor",
@@ -571,7 +563,7 @@ def main():
                      "ms_per_launch": comp_ms["attention"]},
         "score_topk_roofline": st_roof,
         "components_ms": comp_ms,
-        "score_scratch_bytes": score_scratch_bytes(wl, tile, buffers),
+        "score_scratch_bytes": score_scratch_bytes(wl, tile),
         "gpu_launches": args.steps * launches_per_step,
         "clocks": clocks,
         "wall_s_timed_region": wall,

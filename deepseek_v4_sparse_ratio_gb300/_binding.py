@@ -228,7 +228,7 @@ class PrefillWorkspace:
     """Device buffers for dsa_prefill_chunk_host (torch allocations, caller-owned)."""
 
     def __init__(self, max_chunk: int, max_topk: int, raw_kv_rows: int, n_pooled_max: int,
-                 tile_rows: int, device="cuda", tile_buffers: int = 1):
+                 tile_rows: int, device="cuda"):
         dev = torch.device(device)
         self.raw_kv = torch.empty(raw_kv_rows, DIM, dtype=torch.bfloat16, device=dev)
         self.raw_ik = torch.empty(max_chunk, INDEX_DIM, dtype=torch.bfloat16, device=dev)
@@ -238,7 +238,7 @@ class PrefillWorkspace:
         self.q = torch.empty(max_chunk, HEADS, DIM, dtype=torch.bfloat16, device=dev)
         self.sel = torch.empty(max_chunk, max_topk, dtype=torch.int32, device=dev)
         self.out = torch.empty(max_chunk, HEADS, DIM, dtype=torch.bfloat16, device=dev)
-        nbytes = tile_buffers * dsa_score_scratch_bytes(min(tile_rows, max_chunk), n_pooled_max)
+        nbytes = dsa_score_scratch_bytes(min(tile_rows, max_chunk), n_pooled_max)
         self.scratch = torch.empty(max(nbytes // 4, 1), dtype=torch.float32, device=dev)
         self.c = dsa_prefill_workspace(
             self.raw_kv.data_ptr(), raw_kv_rows, self.raw_ik.data_ptr(), self.q_idx.data_ptr(),

@@ -67,13 +67,9 @@ int check_score_topk(const void *q_idx, const float *w, const void *pooled_ik, i
                      const void *scratch, size_t scratch_bytes, const int32_t *sel);
 int prepare_score_topk(const void *q_idx, const void *pooled_ik, int64_t n, int64_t chunk,
                        int32_t k, ScoreTopkPlan *plan);
-// With scratch_bytes of at least two tiles and more than one tile, the tiles
-// ping-pong between the two halves (tile i's top-k runs inside tile i+1's score
-// kernel); otherwise they run one after another in one buffer.
 int enqueue_score_topk(const ScoreTopkPlan &plan, const float *w, int64_t n, int64_t chunk,
                        int64_t offset, int32_t ratio, int32_t k, int64_t tile_rows,
-                       void *scratch, size_t scratch_bytes, int32_t *sel, int32_t *status,
-                       cudaStream_t s);
+                       void *scratch, int32_t *sel, int32_t *status, cudaStream_t s);
 
 // Window + selected attention (step d).
 struct AttnPlan {

@@ -53,8 +53,8 @@ void advance_state(dsa_pool_state *st, int64_t end) {
 int enqueue_pool_and_select(const dsa_pool_state *st, const ScoreTopkPlan &plan,
                             const void *raw_kv, int64_t raw_start, const void *raw_ik,
                             const float *w, int64_t chunk, int64_t offset, int32_t index_topk,
-                            int64_t tile_rows, void *scratch, size_t scratch_bytes, int32_t *sel,
-                            int32_t *status, cudaStream_t s) {
+                            int64_t tile_rows, void *scratch, int32_t *sel, int32_t *status,
+                            cudaStream_t s) {
     const int32_t ratio = st->ratio;
     const int64_t n = (offset + chunk) / ratio;
     const void *chunk_kv =
@@ -62,7 +62,7 @@ int enqueue_pool_and_select(const dsa_pool_state *st, const ScoreTopkPlan &plan,
     int rc = launch_pool_append(*st, chunk_kv, raw_ik, chunk, offset, s);
     if (rc != DSA_OK) return rc;
     return enqueue_score_topk(plan, w, n, chunk, offset, ratio, index_topk, tile_rows, scratch,
-                              scratch_bytes, sel, status, s);
+                              sel, status, s);
 }
 
 }  // namespace
@@ -88,8 +88,7 @@ extern "C" int dsa_prefill_chunk(dsa_pool_state *st, const void *raw_kv, int64_t
     if (rc != DSA_OK) return rc;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     rc = enqueue_pool_and_select(st, splan, raw_kv, raw_start, raw_ik, w, chunk, offset,
-                                 index_topk, tile_rows, scratch, scratch_bytes, sel, dev_status,
-                                 s);
+                                 index_topk, tile_rows, scratch, sel, dev_status, s);
     if (rc == DSA_OK)
         rc = enqueue_attention(aplan, raw_kv, raw_start, st->pooled_kv, n, sel, index_topk, chunk,
                                offset, st->ratio, window, scale, out, dev_status, s);
@@ -189,8 +188,8 @@ extern "C" int dsa_prefill_chunk_host(dsa_pool_state *st, const dsa_prefill_work
     if (!ok) return DSA_ERR_CUDA;
 
     rc = enqueue_pool_and_select(st, splan, ws->raw_kv, raw_start, ws->raw_ik, ws->w, chunk,
-                                 offset, index_topk, tile_rows, ws->scratch, ws->scratch_bytes,
-                                 ws->sel, dev_status, s);
+                                 offset, index_topk, tile_rows, ws->scratch, ws->sel,
+                                 dev_status, s);
     if (rc != DSA_OK) return rc;
     ok = ok && cudaEventRecord(sel_done, s) == cudaSuccess;
     ok = ok && cudaStreamWaitEvent(c, sel_done, 0) == cudaSuccess;

@@ -48,11 +48,9 @@ namespace {
 
 // ------------------------------------------------------------------ top-k helpers
 //
-// The top-k runs either as CTAs of its own (topk_kernel) or as a group of warps
-// inside the score kernel that selects the rows of the tile before (ping-pong
-// scratch). The helpers below work for a group of NT threads: `tid` is the
-// thread's index in the group (the group starts at a warp boundary) and `sync`
-// is the group's barrier.
+// The helpers below work for a group of NT threads: `tid` is the thread's index
+// in the group (the group starts at a warp boundary) and `sync` is the group's
+// barrier (the whole CTA here).
 
 constexpr int kBins = 2048;
 constexpr int kCandCap = 2048;
@@ -398,10 +396,7 @@ __device__ void topk_row_vec(const float *__restrict__ src, int64_t L, int32_t k
 constexpr int kTok = 8;            // query rows per work unit
 constexpr int kStages = 2;         // key-block ring depth
 constexpr int kEpiWarps = 16;      // one 4-row x 32-lane slice of a TMEM half each
-// warp 0 TMA, warp 1 MMA, warps 2-3 the top-k of the previous tile, 4-19 epilogue
-constexpr int kTopkWarp0 = 2;
-constexpr int kTopkGroup = 64;     // threads of the in-kernel top-k group
-constexpr int kEpiWarp0 = 4;
+constexpr int kEpiWarp0 = 2;       // warp 0 TMA, warp 1 MMA, warps 2-17 epilogue
 constexpr int kScoreThreads = 32 * (kEpiWarp0 + kEpiWarps);
 constexpr uint32_t kBBytes = 2 * 2 * 256 * 128;  // [half][k-chunk][256 rows][128 B]
 constexpr uint32_t kAStage = 2 * 128 * 128;      // [k-chunk][128 rows][128 B]
@@ -409,9 +404,7 @@ constexpr uint32_t kOffB = 0;
 constexpr uint32_t kOffA = kOffB + kBBytes;
 constexpr uint32_t kOffW = kOffA + kStages * kAStage;
 constexpr uint32_t kOffRng = kOffW + kTok * kHI * 4;  // [16 epilogue warps][4] partial ranges
-constexpr uint32_t kOffTopk = kOffRng + kEpiWarps * 4 * 4;
-constexpr uint32_t kOffBar =
-    kOffTopk + (static_cast<uint32_t>(sizeof(TopkShared<kTopkGroup>)) + 15u) / 16u * 16u;
+constexpr uint32_t kOffBar = kOffRng + kEpiWarps * 4 * 4;
 constexpr uint32_t kScoreSmem = kOffBar + 256 + 1024;  // + slack for 1024-B alignment
 static_assert(kScoreSmem <= 232448, "over the shared memory of one CTA");
 
@@ -430,14 +423,6 @@ struct ScoreParams {
     int32_t *rng;     // selection rows [chunk, k] used as range scratch, or null
     int32_t k;        // selection row length
     int32_t *status;
-    // the previous tile, whose top-k the kernel's top-k warps run (ping-pong scratch):
-    // its scores (the other half of the scratch), first chunk row, rows (0: none) and
-    // the segment count of its parked row ranges (0: none)
-    const float *prev_scores;
-    int64_t prev_r0;
-    int prev_R;
-    int prev_nseg;
-    int32_t *sel;     // selection [chunk, k]
 };
 
 struct Unit {
@@ -605,25 +590,6 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
         // every MMA issued above must have finished before TMEM is released
         mma_commit(drain);
         drain_wait(drain, 0);
-    } else if (warp >= kTopkWarp0 && warp < kEpiWarp0) {
-        // ---------------- top-k of the previous tile's rows (its scores sit in the other
-        // half of the scratch), last rows first, spread over the CTAs
-        TopkShared<kTopkGroup> &sh = *reinterpret_cast<TopkShared<kTopkGroup> *>(smem + kOffTopk);
-        const int tid = threadIdx.x - 32 * kTopkWarp0;
-        for (int it = blockIdx.x; it < p.prev_R; it += gridDim.x) {
-            const int row = p.prev_R - 1 - it;
-            const int64_t t = p.offset + p.prev_r0 + row;
-            const int64_t L = min(p.n, (t + 1) / p.ratio);
-            int32_t *out = p.sel + (p.prev_r0 + row) * static_cast<int64_t>(p.k);
-            if (L <= p.k) {
-                for (int i = tid; i < p.k; i += kTopkGroup) out[i] = i < L ? i : -1;
-                continue;
-            }
-            topk_row_vec<kTopkGroup, 8>(p.prev_scores + static_cast<int64_t>(row) * p.stride, L,
-                                        p.k, p.prev_nseg, out, sh, tid,
-                                        GroupSync<2, kTopkGroup>{});
-            GroupSync<2, kTopkGroup>{}();  // the shared arrays are reused by the next row
-        }
     } else if (warp >= kEpiWarp0) {
         // ---------------- epilogue: 16 warps; warp reads TMEM sub-partition sp = warp % 4
         // (pooled rows j = 32sp .. 32sp+31 of the block) for token tl of each 4-token half
@@ -941,6 +907,30 @@ __global__ void __launch_bounds__(NT)
     }
 }
 
+// Long rows: a persistent CTA per SM (or fewer) walks rows R-1-blockIdx.x,
+// R-1-blockIdx.x-gridDim.x, ... with 16-byte loads (topk_row_vec). Few rows are in
+// flight at once, so the passes after the first find the row in L2.
+template <int NT, int U>
+__global__ void __launch_bounds__(NT)
+    topk_vec_kernel(const float *__restrict__ scores, int64_t stride, int64_t n, int64_t offset,
+                    int32_t ratio, int64_t r0, int R, int32_t k, int32_t nseg,
+                    int32_t *__restrict__ sel) {
+    __shared__ TopkShared<NT> sh;
+    for (int it = blockIdx.x; it < R; it += gridDim.x) {
+        const int row = R - 1 - it;
+        const int64_t t = offset + r0 + row;
+        const int64_t L = min(n, (t + 1) / ratio);
+        int32_t *out = sel + (r0 + row) * static_cast<int64_t>(k);
+        if (L <= k) {
+            for (int i = threadIdx.x; i < k; i += NT) out[i] = i < L ? i : -1;
+        } else {
+            topk_row_vec<NT, U>(scores + static_cast<int64_t>(row) * stride, L, k, nseg, out, sh,
+                                threadIdx.x, CtaSync{});
+        }
+        __syncthreads();  // the shared arrays are reused by the next row
+    }
+}
+
 // Selection without scoring: sel[i, c] = c if c < n_vis(t) else -1 (n = 0: all -1).
 // One CTA per row; 16-byte stores of four entries when k is a multiple of 4.
 __global__ void __launch_bounds__(256) fill_selection_kernel(int32_t *sel, int32_t k,
@@ -988,13 +978,10 @@ int launch_fill_selection(int32_t *sel, int64_t rows, int32_t k, int64_t offset,
     return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
-// Scores of tile rows [r0, r0 + R) into `scores`; with prev_R > 0 the kernel's
-// top-k warps also select the rows [prev_r0, prev_r0 + prev_R) of the previous
-// tile from prev_scores (prev_nseg: that tile's parked range count).
+// Scores of tile rows [r0, r0 + R) into `scores`.
 int launch_score_tile(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const float *w, int64_t n,
                       int64_t offset, int32_t ratio, int64_t r0, int64_t R, float *scores,
                       int64_t stride, int32_t *sel, int32_t k, int *nseg_rng, int32_t *status,
-                      const float *prev_scores, int64_t prev_r0, int64_t prev_R, int prev_nseg,
                       cudaStream_t s) {
     const int sms = std::max(1, sm_count());
     ScoreParams p;
@@ -1016,11 +1003,6 @@ int launch_score_tile(const CUtensorMap &tm_q, const CUtensorMap &tm_k, const fl
     p.k = k;
     if (nseg_rng) *nseg_rng = rng ? p.nseg : 0;
     p.status = status;
-    p.prev_scores = prev_scores;
-    p.prev_r0 = prev_r0;
-    p.prev_R = static_cast<int>(prev_R);
-    p.prev_nseg = prev_nseg;
-    p.sel = sel;
     const int grid = std::min(p.n_units, sms);
     score_kernel<<<grid, kScoreThreads, kScoreSmem, s>>>(tm_q, tm_k, p);
     return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
@@ -1030,15 +1012,22 @@ int launch_topk_tile(const float *scores, int64_t stride, int64_t n, int64_t off
                      int32_t ratio, int64_t r0, int64_t R, int32_t k, int32_t nseg_rng,
                      int32_t *sel, int32_t *status, cudaStream_t s) {
     (void)status;
-    // 1024-thread CTAs (one per SM) for tiles of few rows, and for long rows: with
-    // rows over 64K scores (256 KB) four CTAs per SM would keep more rows in flight
-    // than L2 holds, and every pass after the first would go back to HBM
-    if (R < 2 * static_cast<int64_t>(sm_count()) || n > 65536)
+    const int sms = std::max(1, sm_count());
+    if (n > 65536) {
+        // rows over 64K scores (256 KB): one persistent 1024-thread CTA on half the SMs,
+        // so the rows in flight (one per CTA) stay well inside L2 for the passes after
+        // the first
+        const int grid = static_cast<int>(std::min<int64_t>(R, std::max(1, sms / 2)));
+        topk_vec_kernel<kTopkThreadsFew, 4><<<grid, kTopkThreadsFew, 0, s>>>(
+            scores, stride, n, offset, ratio, r0, static_cast<int>(R), k, nseg_rng, sel);
+    } else if (R < 2 * static_cast<int64_t>(sms)) {
+        // few rows (decode steps, short bands): 1024-thread CTAs walk each row faster
         topk_kernel<kTopkThreadsFew><<<static_cast<unsigned>(R), kTopkThreadsFew, 0, s>>>(
             scores, stride, n, offset, ratio, r0, k, nseg_rng, sel);
-    else
+    } else {
         topk_kernel<kTopkThreads><<<static_cast<unsigned>(R), kTopkThreads, 0, s>>>(
             scores, stride, n, offset, ratio, r0, k, nseg_rng, sel);
+    }
     return cudaGetLastError() == cudaSuccess ? DSA_OK : DSA_ERR_CUDA;
 }
 
@@ -1099,48 +1088,20 @@ int prepare_score_topk(const void *q_idx, const void *pooled_ik, int64_t n, int6
 
 int enqueue_score_topk(const ScoreTopkPlan &plan, const float *w, int64_t n, int64_t chunk,
                        int64_t offset, int32_t ratio, int32_t k, int64_t tile_rows,
-                       void *scratch, size_t scratch_bytes, int32_t *sel, int32_t *status,
-                       cudaStream_t s) {
+                       void *scratch, int32_t *sel, int32_t *status, cudaStream_t s) {
     if (!plan.full) return launch_fill_selection(sel, chunk, k, offset, n, ratio, s);
     const int64_t stride = score_stride(n);
     float *scores = static_cast<float *>(scratch);
-    const int64_t tile = std::min(tile_rows, chunk);
-    // Two tile buffers in the scratch and more than one tile: ping-pong. The score
-    // kernel of tile i writes one buffer while its top-k warps select tile i-1 from
-    // the other; only the last tile's top-k runs on its own.
-    const bool pingpong =
-        chunk > tile && scratch_bytes / 2 >= dsa_score_scratch_bytes(tile, n);
-    if (!pingpong) {
-        for (int64_t r0 = 0; r0 < chunk; r0 += tile) {
-            const int64_t R = std::min(tile, chunk - r0);
-            int nseg_rng = 0;
-            int rc = launch_score_tile(plan.tm_q, plan.tm_k, w, n, offset, ratio, r0, R, scores,
-                                       stride, sel, k, &nseg_rng, status, nullptr, 0, 0, 0, s);
-            if (rc != DSA_OK) return rc;
-            rc = launch_topk_tile(scores, stride, n, offset, ratio, r0, R, k, nseg_rng, sel,
-                                  status, s);
-            if (rc != DSA_OK) return rc;
-        }
-        return DSA_OK;
-    }
-    const int64_t half = tile * stride;  // floats of one tile buffer
-    int64_t prev_r0 = 0, prev_R = 0;
-    int prev_nseg = 0, i = 0;
-    for (int64_t r0 = 0; r0 < chunk; r0 += tile, ++i) {
-        const int64_t R = std::min(tile, chunk - r0);
-        float *buf = scores + (i & 1) * half;
-        const float *prev = scores + ((i + 1) & 1) * half;
+    for (int64_t r0 = 0; r0 < chunk; r0 += tile_rows) {
+        const int64_t R = std::min(tile_rows, chunk - r0);
         int nseg_rng = 0;
-        int rc = launch_score_tile(plan.tm_q, plan.tm_k, w, n, offset, ratio, r0, R, buf, stride,
-                                   sel, k, &nseg_rng, status, prev, prev_r0, prev_R, prev_nseg,
-                                   s);
+        int rc = launch_score_tile(plan.tm_q, plan.tm_k, w, n, offset, ratio, r0, R, scores,
+                                   stride, sel, k, &nseg_rng, status, s);
         if (rc != DSA_OK) return rc;
-        prev_r0 = r0;
-        prev_R = R;
-        prev_nseg = nseg_rng;
+        rc = launch_topk_tile(scores, stride, n, offset, ratio, r0, R, k, nseg_rng, sel, status, s);
+        if (rc != DSA_OK) return rc;
     }
-    return launch_topk_tile(scores + ((i + 1) & 1) * half, stride, n, offset, ratio, prev_r0,
-                            prev_R, k, prev_nseg, sel, status, s);
+    return DSA_OK;
 }
 
 }  // namespace dsa
@@ -1164,8 +1125,7 @@ extern "C" int dsa_index_score_topk(const void *q_idx, const float *w, const voi
     rc = prepare_score_topk(q_idx, pooled_ik, n_pooled, chunk, index_topk, &plan);
     if (rc != DSA_OK) return rc;
     return enqueue_score_topk(plan, w, n_pooled, chunk, offset, ratio, index_topk, tile_rows,
-                              scratch, scratch_bytes, sel, dev_status,
-                              static_cast<cudaStream_t>(stream));
+                              scratch, sel, dev_status, static_cast<cudaStream_t>(stream));
 }
 
 // ------------------------------------------------------------------ no-allocation variant
@@ -1255,9 +1215,6 @@ extern "C" int dsa_index_score_topk_noalloc(const void *q_idx, const float *w,
     ScoreTopkPlan plan;
     rc = prepare_score_topk(q_idx, pooled_ik, n_pooled, chunk, index_topk, &plan);
     if (rc != DSA_OK) return rc;
-    // one tile buffer: the tiles run one after another, as with a one-tile caller scratch
-    const size_t one_tile = dsa_score_scratch_bytes(std::min(tile_rows, chunk), n_pooled);
     return enqueue_score_topk(plan, w, n_pooled, chunk, offset, ratio, index_topk, tile_rows,
-                              scratch, one_tile, sel, dev_status,
-                              static_cast<cudaStream_t>(stream));
+                              scratch, sel, dev_status, static_cast<cudaStream_t>(stream));
 }

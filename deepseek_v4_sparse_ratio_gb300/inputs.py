@@ -44,7 +44,6 @@ class Workload:
     ratio: int = RATIO
     sample_rows: int = 0  # oracle rows to check per chunk at full size (0 = all)
     tile_rows: tuple = ()  # indexer tile sizes the workload is run with
-    tile_buffers: int = 1  # score-scratch tile buffers of the benchmark run (2: ping-pong)
     t: dict = field(default_factory=dict)
 
     @property

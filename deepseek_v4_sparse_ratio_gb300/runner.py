@@ -17,7 +17,7 @@ from .inputs import Workload
 
 class DeviceWorkload:
     def __init__(self, wl: Workload, tile_rows: int | None = None, device="cuda",
-                 keep_outputs: bool = False, tile_buffers: int = 1):
+                 keep_outputs: bool = False):
         self.wl = wl
         t = wl.t
         dev = torch.device(device)
@@ -36,9 +36,7 @@ class DeviceWorkload:
         self.k = wl.index_topk
         self.tile_rows = tile_rows or (wl.tile_rows[0] if wl.tile_rows else self.tmax)
         n_final = wl.end // wl.ratio
-        # tile_buffers = 2: room for two tiles, so the indexer's tiles ping-pong (the
-        # top-k of one tile runs inside the score kernel of the next)
-        nbytes = tile_buffers * B.dsa_score_scratch_bytes(min(self.tile_rows, self.tmax), n_final)
+        nbytes = B.dsa_score_scratch_bytes(min(self.tile_rows, self.tmax), n_final)
         self.scratch = torch.empty(max(nbytes // 4, 1), dtype=torch.float32, device=dev)
         self.sel = torch.empty(self.tmax, self.k, dtype=torch.int32, device=dev)
         self.out = torch.empty(self.tmax, B.HEADS, B.DIM, dtype=torch.bfloat16, device=dev)

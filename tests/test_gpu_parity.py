@@ -189,50 +189,41 @@ def test_topk_heavy_ties_on_every_selection_path(dsa, L, m, k, T):
     assert np.array_equal(sel.cpu().numpy(), oracle.topk(gpu_s, pos, n, 4, k))
 
 
-@pytest.mark.parametrize("off,T,k,tile", [(4096, 1000, 256, 333), (20000, 700, 512, 64),
-                                          (8188, 37, 100, 16), (280000, 320, 2048, 100),
-                                          (4096, 1000, 256, 999)])
-def test_pingpong_tiles_match_one_buffer_and_oracle(dsa, off, T, k, tile):
-    """A scratch of two tiles: the score kernel of each tile runs the top-k of the
-    tile before in its own warps (16-byte loads, a 64-thread group), and the last
-    tile's top-k runs alone. The selection must equal the one-buffer run's bit for
-    bit and pass the oracle on every row; the last tile's scores sit in its half
-    of the scratch and are compared element by element."""
+@pytest.mark.parametrize("off,T,k,tile", [(280000, 37, 2048, 16), (300004, 160, 1000, 160),
+                                          (262150, 90, 64, 31)])
+def test_long_rows_match_oracle(dsa, off, T, k, tile):
+    """Rows over 65,536 pooled rows take the persistent top-k (16-byte loads, one
+    1024-thread CTA walking several rows): ragged row lengths (n_vis not a multiple
+    of the 128-score pieces), tiles whose rows outnumber the CTAs, scores compared
+    element by element and the selection against the oracle on every row."""
     q_idx, w, pik, n = _score_case(off + T + tile, off, T, k)
-    args = [t.cuda() for t in (q_idx, w, pik)]
-    one = B.dsa_score_scratch_bytes(tile, n)
-    sels = []
-    for buffers in (1, 2):
-        sel = torch.full((T, k), 7, dtype=torch.int32, device="cuda")
-        scratch = torch.empty(buffers * one // 4, dtype=torch.float32, device="cuda")
-        status = torch.zeros(1, dtype=torch.int32, device="cuda")
-        B.dsa_index_score_topk(*args, n, T, off, 4, k, tile, scratch, sel, status)
-        torch.cuda.synchronize()
-        assert status.item() == 0
-        sels.append(sel.cpu())
-    assert torch.equal(sels[0], sels[1])
+    assert n > 65536
+    sel = torch.full((T, k), 7, dtype=torch.int32, device="cuda")
+    scratch = torch.empty(B.dsa_score_scratch_bytes(tile, n) // 4, dtype=torch.float32,
+                          device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.dsa_index_score_topk(q_idx.cuda(), w.cuda(), pik.cuda(), n, T, off, 4, k, tile, scratch,
+                           sel, status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
     pos = off + np.arange(T)
     ref_s, mag = oracle.index_scores(q_idx, w.numpy(), pos, pik, n)
-    ref_sel = oracle.topk(ref_s, pos, n, 4, k)
-    check_selection(sels[1].numpy(), ref_sel, pos, n, k, ref_s, mag)
-    # the last tile (index ntiles-1) was written to half (ntiles-1) % 2
+    check_selection(sel.cpu().numpy(), oracle.topk(ref_s, pos, n, 4, k), pos, n, k, ref_s, mag)
     stride = (n + 127) // 128 * 128
-    ntiles = (T + tile - 1) // tile
-    last0 = (ntiles - 1) * tile
-    half = ((ntiles - 1) % 2) * tile * stride
-    gs = scratch[half: half + (T - last0) * stride].view(T - last0, stride)[:, :n].cpu().numpy()
+    last0 = ((T - 1) // tile) * tile
+    gs = scratch[: (T - last0) * stride].view(T - last0, stride)[:, :n].cpu().numpy()
     check_scores(gs, ref_s[last0:], mag[last0:])
 
 
-@pytest.mark.parametrize("L,m,k,T", [(4000, 30, 64, 320), (4000, 600, 300, 320),
-                                     (4000, 100, 3000, 320), (70000, 100, 64, 320),
+@pytest.mark.parametrize("L,m,k,T", [(70000, 30, 64, 320), (70000, 600, 300, 320),
+                                     (70000, 1500, 1024, 320), (70000, 100, 3000, 320),
                                      (70000, 3000, 2048, 96)])
-def test_pingpong_topk_heavy_ties(dsa, L, m, k, T):
-    """The heavy-tie rows of test_topk_heavy_ties_on_every_selection_path through the
-    ping-pong path (tiles of T/4 rows, two tile buffers): the in-kernel top-k group
-    ranks up to 64 candidates against each other, radix-selects a crowded bin, or
-    radix-selects the whole row when the bin overflows. Checked against the oracle's
-    top-k of the GPU's own scores, exactly."""
+def test_long_row_topk_heavy_ties_in_tiles(dsa, L, m, k, T):
+    """Heavy-tie rows of 70,000 scores through the persistent long-row top-k, in
+    tiles of T/4 rows (each CTA walks several rows): a few candidates ranked against
+    each other, a crowded bin radix-selected, and a bin too crowded to collect
+    (radix select over the row). Checked against the oracle's top-k of the GPU's
+    own scores, exactly, and against a one-tile run."""
     g = torch.Generator().manual_seed(L + m + k + 1)
     off = 4 * L
     n = (off + T) // 4
@@ -245,13 +236,12 @@ def test_pingpong_topk_heavy_ties(dsa, L, m, k, T):
     pik = pik.to(torch.bfloat16)
     tile = T // 4
     sel = torch.empty(T, k, dtype=torch.int32, device="cuda")
-    one = B.dsa_score_scratch_bytes(tile, n)
-    scratch = torch.empty(2 * one // 4, dtype=torch.float32, device="cuda")
+    scratch = torch.empty(B.dsa_score_scratch_bytes(tile, n) // 4, dtype=torch.float32,
+                          device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     B.dsa_index_score_topk(q_idx.cuda(), w.cuda(), pik.cuda(), n, T, off, 4, k, tile, scratch,
                            sel, status)
-    # the scores of every row, for the exact replay: a one-tile-per-row-set rerun
-    # would change nothing, so recompute them in one buffer per tile
+    # the scores of every row for the exact replay, from a one-tile run
     full = torch.empty(B.dsa_score_scratch_bytes(T, n) // 4, dtype=torch.float32, device="cuda")
     sel1 = torch.empty(T, k, dtype=torch.int32, device="cuda")
     B.dsa_index_score_topk(q_idx.cuda(), w.cuda(), pik.cuda(), n, T, off, 4, k, T, full, sel1,
