@@ -724,6 +724,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
 // enough to fill the GPU and the rows are short, else 1024
 constexpr int kTopkThreads = 256;
 constexpr int kTopkThreadsFew = 1024;
+constexpr int kTopkThreadsLong = 512;   // persistent CTAs for rows over 64K scores
 
 // One CTA per query row; every pass walks the row in per-warp contiguous
 // segments (coalesced, and the last pass must emit in index order). Rows are
@@ -1014,11 +1015,12 @@ int launch_topk_tile(const float *scores, int64_t stride, int64_t n, int64_t off
     (void)status;
     const int sms = std::max(1, sm_count());
     if (n > 65536) {
-        // rows over 64K scores (256 KB): one persistent 1024-thread CTA on half the SMs,
-        // so the rows in flight (one per CTA) stay well inside L2 for the passes after
-        // the first
-        const int grid = static_cast<int>(std::min<int64_t>(R, std::max(1, sms / 2)));
-        topk_vec_kernel<kTopkThreadsFew, 4><<<grid, kTopkThreadsFew, 0, s>>>(
+        // rows over 64K scores (256 KB): two persistent 512-thread CTAs per SM with
+        // 16-byte loads (a sweep at 1M context: 2 x 512 beat 1 x 1024 per SM, and both
+        // beat fewer CTAs that would keep fewer rows in flight; the kernel is bound by
+        // each SM's loads in flight, not by HBM)
+        const int grid = static_cast<int>(std::min<int64_t>(R, 2 * sms));
+        topk_vec_kernel<kTopkThreadsLong, 4><<<grid, kTopkThreadsLong, 0, s>>>(
             scores, stride, n, offset, ratio, r0, static_cast<int>(R), k, nseg_rng, sel);
     } else if (R < 2 * static_cast<int64_t>(sms)) {
         // few rows (decode steps, short bands): 1024-thread CTAs walk each row faster
