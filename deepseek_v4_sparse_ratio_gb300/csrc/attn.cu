@@ -157,6 +157,16 @@ __device__ __forceinline__ void bar_group(int hh) {
 
 __device__ __forceinline__ void bar_soft() { asm volatile("bar.sync 3, 256;" ::: "memory"); }
 
+// A 16-byte global load issued where it stands: volatile, so the compiler neither
+// moves it nor re-issues it later in place of keeping its registers.
+__device__ __forceinline__ uint4 ld_keep16(const void *src) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(src));
+    return v;
+}
+
 __device__ __forceinline__ void st_shared16(uint32_t dst, const uint4 &v) {
     asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x), "r"(v.y),
                  "r"(v.z), "r"(v.w)
@@ -392,8 +402,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 for (int gq = 0; gq < kMaxGroups; ++gq) {
                     if (gq < ngroups) {
                         const int srow = __shfl_sync(0xFFFFFFFFu, row, 4 * gq + a);
-                        c6[gq] = __ldg(reinterpret_cast<const uint4 *>(
-                            src_base + static_cast<int64_t>(srow) * (kD * 2) + 6 * 128));
+                        c6[gq] = ld_keep16(
+                            src_base + static_cast<int64_t>(srow) * (kD * 2) + 6 * 128);
                     }
                 }
                 // chunk pairs 0-2 by cp.async, then chunk 6 from the registers, as the

@@ -168,26 +168,23 @@ __device__ __forceinline__ void radix_select(KeyAt key_at, int64_t count, uint32
     *need_out = need;
 }
 
-// Top-k of one score row (L visible scores, L > k) by a group of NT threads,
-// with U 16-byte loads in flight per thread in every pass. The same algorithm
-// as topk_kernel: 2048 linear bins between the row's min and max (from the
-// score kernel's segment ranges parked in out[2s], out[2s+1] when nseg > 0),
-// the threshold bin's scores as candidates (ranked against each other, or
-// radix-selected when crowded, or a radix select over the whole row when the
-// bin overflows), then emission of the kept indices in index order. Each warp
-// owns a contiguous segment of whole 128-score pieces; within a piece lane l
-// holds scores 4l..4l+3, and a warp prefix sum orders the emitted indices.
-template <int NT, int U, class Sync>
-__device__ void topk_row_vec(const float *__restrict__ src, int64_t L, int32_t k, int32_t nseg,
-                             int32_t *__restrict__ out, TopkShared<NT> &sh, int tid, Sync sync) {
-    constexpr int NW = NT / 32;
-    const int lane = tid & 31, warp = tid >> 5;
-    const int64_t seg = ((L + NW - 1) / NW + 127) / 128 * 128;
-    const int64_t lo = min(L, seg * warp), hi = min(L, seg * (warp + 1));
-    // every pass: U pieces of 128 scores per warp in flight, visited in index order
-    // (lanes whose 4 scores start at or beyond hi see nothing; within a load, scores
-    // at or beyond hi are masked by the visitor)
-    auto walk = [&](auto &&visit, bool last_pass) {
+// Per-warp contiguous segments of whole 128-score pieces of one row; within a
+// piece lane l holds scores 4l..4l+3 (one 16-byte load). walk() visits the
+// warp's segment in index order with U pieces in flight; scores at or beyond hi
+// are the visitor's to mask.
+template <int NT, int U>
+struct RowWalk {
+    const float *src;
+    int64_t seg, lo, hi;
+    int lane;
+    __device__ __forceinline__ RowWalk(const float *s, int64_t L, int tid) : src(s), lane(tid & 31) {
+        constexpr int NW = NT / 32;
+        seg = ((L + NW - 1) / NW + 127) / 128 * 128;
+        lo = min(L, seg * (tid >> 5));
+        hi = min(L, seg * ((tid >> 5) + 1));
+    }
+    template <class Visit>
+    __device__ __forceinline__ void walk(Visit &&visit, bool last_pass) const {
         for (int64_t base = lo; base < hi; base += 128 * U) {
             float4 v[U];
 #pragma unroll
@@ -200,10 +197,22 @@ __device__ void topk_row_vec(const float *__restrict__ src, int64_t L, int32_t k
 #pragma unroll
             for (int u = 0; u < U; ++u) visit(base + 128 * u + 4 * lane, v[u]);
         }
-    };
-    auto elem = [](const float4 &v, int e) { return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w; };
+    }
+};
 
-    // ---- 1. range of the row
+__device__ __forceinline__ float elem4(const float4 &v, int e) {
+    return e == 0 ? v.x : e == 1 ? v.y : e == 2 ? v.z : v.w;
+}
+
+// The row's (min, max): from the score kernel's segment ranges parked in
+// out[2s], out[2s+1] when nseg > 0, else a pass over the row. Also zeroes the
+// histogram and the candidate count.
+template <int NT, int U, class Sync>
+__device__ __forceinline__ void row_range(const RowWalk<NT, U> &rw, int32_t nseg,
+                                          const int32_t *out, TopkShared<NT> &sh, int tid,
+                                          Sync sync, float *vmin_out, float *vmax_out) {
+    constexpr int NW = NT / 32;
+    const int lane = tid & 31, warp = tid >> 5;
     float vmin = INFINITY, vmax = -INFINITY;
     if (nseg > 0) {
         if (warp == 0)
@@ -212,12 +221,12 @@ __device__ void topk_row_vec(const float *__restrict__ src, int64_t L, int32_t k
                 vmax = fmaxf(vmax, __int_as_float(out[2 * sg + 1]));
             }
     } else {
-        walk([&](int64_t j, const float4 &v) {
+        rw.walk([&](int64_t j, const float4 &v) {
 #pragma unroll
             for (int e = 0; e < 4; ++e)
-                if (j + e < hi) {
-                    vmin = fminf(vmin, elem(v, e));
-                    vmax = fmaxf(vmax, elem(v, e));
+                if (j + e < rw.hi) {
+                    vmin = fminf(vmin, elem4(v, e));
+                    vmax = fmaxf(vmax, elem4(v, e));
                 }
         }, false);
     }
@@ -240,129 +249,37 @@ __device__ void topk_row_vec(const float *__restrict__ src, int64_t L, int32_t k
         vmin = fminf(vmin, sh.s_min[w]);
         vmax = fmaxf(vmax, sh.s_max[w]);
     }
+    *vmin_out = vmin;
+    *vmax_out = vmax;
+}
 
-    uint32_t thr, need_eq;
-    bool counted = false;  // w_gt / w_eq already hold the per-segment counts
-    if (vmin == vmax) {
-        // every visible score is equal: the k lowest indices
-        thr = order_key(vmax);
-        need_eq = static_cast<uint32_t>(k);
-    } else {
-        // ---- 2. linear bins between min and max (monotone: every element of a higher
-        // bin is >= every element of a lower bin)
-        const float scale = static_cast<float>(kBins) / (vmax - vmin);
-        auto bin_of = [&](float v) { return min(kBins - 1, static_cast<int>((v - vmin) * scale)); };
-        walk([&](int64_t j, const float4 &v) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                if (j + e < hi) atomicAdd(&sh.hist[bin_of(elem(v, e))], 1u);
-        }, false);
-        sync();
-        find_bin<NT>(sh.hist, kBins, static_cast<uint32_t>(k), tid, sh.warp_sums, &sh.s_bin,
-                     &sh.s_above, sync);
-        const int bstar = static_cast<int>(sh.s_bin);
-        const uint32_t need = static_cast<uint32_t>(k) - sh.s_above;
-        // ---- 3. the threshold bin's elements are the candidates; each segment's
-        // elements above that bin are counted on the way
-        uint32_t above = 0;
-        walk([&](int64_t j, const float4 &v) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                if (j + e < hi) {
-                    const int b = bin_of(elem(v, e));
-                    above += b > bstar;
-                    if (b == bstar) {
-                        const uint32_t c = atomicAdd(&sh.s_cnt, 1u);
-                        if (c < kCandCap) {
-                            sh.cand[c] = order_key(elem(v, e));
-                            sh.cand_j[c] = static_cast<int32_t>(j + e);
-                        }
-                    }
-                }
-        }, false);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) above += __shfl_xor_sync(0xFFFFFFFFu, above, o);
-        if (lane == 0) {
-            sh.w_gt[warp] = above;
-            sh.w_eq[warp] = 0;
-        }
-        sync();
-        const uint32_t cnt = sh.s_cnt;
-        if (cnt <= NT) {
-            // few candidates: each thread ranks one against all of them; the need-th
-            // largest has fewer than `need` strictly larger keys and at least `need`
-            // larger-or-equal ones
-            if (static_cast<uint32_t>(tid) < cnt) {
-                const uint32_t u = sh.cand[tid];
-                uint32_t gt = 0, ge = 0;
-                for (uint32_t c = 0; c < cnt; ++c) {
-                    const uint32_t w = sh.cand[c];
-                    gt += w > u;
-                    ge += w >= u;
-                }
-                if (gt < need && need <= ge) {  // every thread holding that key agrees
-                    sh.s_bin = u;
-                    sh.s_above = need - gt;
-                }
-            }
-            sync();
-            thr = sh.s_bin;
-            need_eq = sh.s_above;
-        } else if (cnt <= kCandCap) {
-            radix_select<NT>([&](int64_t c) { return sh.cand[c]; }, cnt, need, tid, sh.hist,
-                             sh.warp_sums, &sh.s_bin, &sh.s_above, &thr, &need_eq, sync);
-        }
-        if (cnt <= kCandCap) {
-            // candidates above / equal to the threshold, by segment
-            for (uint32_t c = tid; c < cnt; c += NT) {
-                const int w = static_cast<int>(sh.cand_j[c] / seg);
-                if (sh.cand[c] > thr) atomicAdd(&sh.w_gt[w], 1u);
-                else if (sh.cand[c] == thr) atomicAdd(&sh.w_eq[w], 1u);
-            }
-            sync();
-            counted = true;
-        } else {
-            radix_select<NT>([&](int64_t j) { return order_key(src[j]); }, L,
-                             static_cast<uint32_t>(k), tid, sh.hist, sh.warp_sums, &sh.s_bin,
-                             &sh.s_above, &thr, &need_eq, sync);
-        }
+// Linear bin of v among kBins between vmin and vmax (a monotone map: every element
+// of a higher bin is >= every element of a lower bin).
+struct LinearBins {
+    float vmin, scale;
+    __device__ __forceinline__ int operator()(float v) const {
+        return min(kBins - 1, static_cast<int>((v - vmin) * scale));
     }
+};
 
-    if (!counted) {
-        uint32_t ngt = 0, neq = 0;
-        walk([&](int64_t j, const float4 &v) {
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                if (j + e < hi) {
-                    const uint32_t u = order_key(elem(v, e));
-                    ngt += u > thr;
-                    neq += u == thr;
-                }
-        }, false);
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) {
-            ngt += __shfl_xor_sync(0xFFFFFFFFu, ngt, o);
-            neq += __shfl_xor_sync(0xFFFFFFFFu, neq, o);
-        }
-        if (lane == 0) {
-            sh.w_gt[warp] = ngt;
-            sh.w_eq[warp] = neq;
-        }
-        sync();
-    }
-    // ---- 4. emit kept indices ascending: kept element j goes to
-    // (#above-threshold before j) + min(#equal before j, need_eq)
+// Emission in index order: kept element j goes to (#above-threshold before j) +
+// min(#equal before j, need_eq); w_gt / w_eq hold each warp segment's counts.
+template <int NT, int U>
+__device__ __forceinline__ void emit_ordered(const RowWalk<NT, U> &rw, uint32_t thr,
+                                             uint32_t need_eq, int32_t *out,
+                                             const TopkShared<NT> &sh, int tid) {
+    const int lane = tid & 31, warp = tid >> 5;
     uint32_t base_gt = 0, base_eq = 0;
     for (int w = 0; w < warp; ++w) {
         base_gt += sh.w_gt[w];
         base_eq += sh.w_eq[w];
     }
-    walk([&](int64_t j, const float4 &v) {
+    rw.walk([&](int64_t j, const float4 &v) {
         uint32_t gm = 0, em = 0;
 #pragma unroll
         for (int e = 0; e < 4; ++e)
-            if (j + e < hi) {
-                const uint32_t u = order_key(elem(v, e));
+            if (j + e < rw.hi) {
+                const uint32_t u = order_key(elem4(v, e));
                 gm |= static_cast<uint32_t>(u > thr) << e;
                 em |= static_cast<uint32_t>(u == thr) << e;
             }
@@ -389,6 +306,286 @@ __device__ void topk_row_vec(const float *__restrict__ src, int64_t L, int32_t k
         base_gt += tot & 0xFFFFu;
         base_eq += tot >> 16;
     }, true);
+}
+
+// After the histogram of the row over `bins` is in sh.hist: find the threshold bin,
+// collect its candidates (counting each segment's elements above it), find the exact
+// k-th key and its kept equals (candidate rank, radix select over the candidates, or
+// over the whole row when the bin overflows), and emit in index order.
+template <int NT, int U, class Sync>
+__device__ void topk_finish(const RowWalk<NT, U> &rw, int64_t L, int32_t k, LinearBins bin_of,
+                            int32_t *__restrict__ out, TopkShared<NT> &sh, int tid, Sync sync) {
+    const int lane = tid & 31, warp = tid >> 5;
+    find_bin<NT>(sh.hist, kBins, static_cast<uint32_t>(k), tid, sh.warp_sums, &sh.s_bin,
+                 &sh.s_above, sync);
+    const int bstar = static_cast<int>(sh.s_bin);
+    const uint32_t need = static_cast<uint32_t>(k) - sh.s_above;
+    uint32_t above = 0;
+    rw.walk([&](int64_t j, const float4 &v) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if (j + e < rw.hi) {
+                const int b = bin_of(elem4(v, e));
+                above += b > bstar;
+                if (b == bstar) {
+                    const uint32_t c = atomicAdd(&sh.s_cnt, 1u);
+                    if (c < kCandCap) {
+                        sh.cand[c] = order_key(elem4(v, e));
+                        sh.cand_j[c] = static_cast<int32_t>(j + e);
+                    }
+                }
+            }
+    }, false);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) above += __shfl_xor_sync(0xFFFFFFFFu, above, o);
+    if (lane == 0) {
+        sh.w_gt[warp] = above;
+        sh.w_eq[warp] = 0;
+    }
+    sync();
+    const uint32_t cnt = sh.s_cnt;
+    uint32_t thr, need_eq;
+    bool counted = false;  // w_gt / w_eq already hold the per-segment counts
+    if (cnt <= NT) {
+        // few candidates: each thread ranks one against all of them; the need-th
+        // largest has fewer than `need` strictly larger keys and at least `need`
+        // larger-or-equal ones
+        if (static_cast<uint32_t>(tid) < cnt) {
+            const uint32_t u = sh.cand[tid];
+            uint32_t gt = 0, ge = 0;
+            for (uint32_t c = 0; c < cnt; ++c) {
+                const uint32_t w = sh.cand[c];
+                gt += w > u;
+                ge += w >= u;
+            }
+            if (gt < need && need <= ge) {  // every thread holding that key agrees
+                sh.s_bin = u;
+                sh.s_above = need - gt;
+            }
+        }
+        sync();
+        thr = sh.s_bin;
+        need_eq = sh.s_above;
+    } else if (cnt <= kCandCap) {
+        radix_select<NT>([&](int64_t c) { return sh.cand[c]; }, cnt, need, tid, sh.hist,
+                         sh.warp_sums, &sh.s_bin, &sh.s_above, &thr, &need_eq, sync);
+    } else {
+        radix_select<NT>([&](int64_t j) { return order_key(rw.src[j]); }, L,
+                         static_cast<uint32_t>(k), tid, sh.hist, sh.warp_sums, &sh.s_bin,
+                         &sh.s_above, &thr, &need_eq, sync);
+    }
+    if (cnt <= kCandCap) {
+        // candidates above / equal to the threshold, by segment
+        for (uint32_t c = tid; c < cnt; c += NT) {
+            const int w = static_cast<int>(sh.cand_j[c] / rw.seg);
+            if (sh.cand[c] > thr) atomicAdd(&sh.w_gt[w], 1u);
+            else if (sh.cand[c] == thr) atomicAdd(&sh.w_eq[w], 1u);
+        }
+        sync();
+        counted = true;
+    }
+    if (!counted) {
+        uint32_t ngt = 0, neq = 0;
+        rw.walk([&](int64_t j, const float4 &v) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (j + e < rw.hi) {
+                    const uint32_t u = order_key(elem4(v, e));
+                    ngt += u > thr;
+                    neq += u == thr;
+                }
+        }, false);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            ngt += __shfl_xor_sync(0xFFFFFFFFu, ngt, o);
+            neq += __shfl_xor_sync(0xFFFFFFFFu, neq, o);
+        }
+        if (lane == 0) {
+            sh.w_gt[warp] = ngt;
+            sh.w_eq[warp] = neq;
+        }
+        sync();
+    }
+    emit_ordered<NT, U>(rw, thr, need_eq, out, sh, tid);
+}
+
+// Shared memory of the sample-guided pass: the candidates it collects and a bitmap of
+// the kept indices of a row of up to kBits scores.
+template <int kCap, int kBits>
+struct GuidedShared {
+    uint32_t key[kCap];
+    int32_t idx[kCap];
+    uint32_t bitmap[kBits / 32];
+    uint32_t cnt, n_eq;
+};
+
+// Sample-guided selection of one row (L <= kBits) after its range is known:
+//  1. a sample of whole 128-score pieces spread evenly over the row, binned like the
+//     row, gives a bin tau that lies, with a wide margin, below the bin of the k-th
+//     largest score (the sample's rank k * samples / L plus 3 standard deviations
+//     plus 8);
+//  2. one pass over the row builds the full histogram and collects every score in
+//     bins >= tau (key, index);
+//  3. if the k-th largest lies in a bin >= tau and the candidates fit, it and its
+//     kept equals are found exactly among the candidates (radix select); the kept
+//     indices are set in a bitmap (ties at the threshold: the lowest indices) and
+//     emitted in index order from it, without another pass over the scores.
+// Returns 0 when the row is done; 1 when step 3 does not apply (sh.hist then holds
+// the row's full histogram); 2 when the sample cannot place tau (sh.hist zeroed).
+template <int NT, int U, int kCap, int kBits, class Sync>
+__device__ int topk_guided(const RowWalk<NT, U> &rw, int64_t L, int32_t k, LinearBins bin_of,
+                           int32_t *__restrict__ out, TopkShared<NT> &sh,
+                           GuidedShared<kCap, kBits> &gs, int tid, Sync sync) {
+    constexpr int NW = NT / 32;
+    const int lane = tid & 31, warp = tid >> 5;
+    const int64_t pieces = (L + 127) / 128;
+    const int ns = static_cast<int>(max(int64_t{8}, min(int64_t{64}, L / 4096)));
+    const int64_t words = (L + 31) / 32;
+    for (int64_t w = tid; w < words; w += NT) gs.bitmap[w] = 0;
+    if (tid == 0) {
+        gs.cnt = 0;
+        gs.n_eq = 0;
+    }
+    // ---- 1. the sample (piece c starts at 128 * floor(c * pieces / ns))
+    int64_t samples = 0;
+    for (int c = 0; c < ns; ++c) {
+        const int64_t base = (c * pieces / ns) * 128;
+        samples += min(int64_t{128}, L - base);
+        if (c % NW == warp) {
+            const int64_t j = base + 4 * lane;
+            if (j < L) {
+                const float4 v = __ldcg(reinterpret_cast<const float4 *>(rw.src + j));
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (j + e < L) atomicAdd(&sh.hist[bin_of(elem4(v, e))], 1u);
+            }
+        }
+    }
+    sync();
+    const double expect = static_cast<double>(k) * static_cast<double>(samples) /
+                          static_cast<double>(L);
+    const int64_t need_s = static_cast<int64_t>(ceil(expect + 3.0 * sqrt(expect) + 8.0));
+    int tau = -1;
+    if (need_s < samples) {
+        find_bin<NT>(sh.hist, kBins, static_cast<uint32_t>(need_s), tid, sh.warp_sums, &sh.s_bin,
+                     &sh.s_above, sync);
+        tau = static_cast<int>(sh.s_bin);
+    }
+    for (int i = tid; i < kBins; i += NT) sh.hist[i] = 0;
+    sync();
+    if (tau < 0) return 2;
+    // ---- 2. full histogram, candidates of bins >= tau
+    rw.walk([&](int64_t j, const float4 &v) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if (j + e < rw.hi) {
+                const int b = bin_of(elem4(v, e));
+                atomicAdd(&sh.hist[b], 1u);
+                if (b >= tau) {
+                    const uint32_t c = atomicAdd(&gs.cnt, 1u);
+                    if (c < kCap) {
+                        gs.key[c] = order_key(elem4(v, e));
+                        gs.idx[c] = static_cast<int32_t>(j + e);
+                    }
+                }
+            }
+    }, false);
+    sync();
+    find_bin<NT>(sh.hist, kBins, static_cast<uint32_t>(k), tid, sh.warp_sums, &sh.s_bin,
+                 &sh.s_above, sync);
+    const uint32_t cnt = gs.cnt;
+    if (static_cast<int>(sh.s_bin) < tau || cnt > static_cast<uint32_t>(kCap)) return 1;
+    // ---- 3. every score of the bins >= tau is a candidate, so the k-th largest score
+    // overall is the k-th largest candidate
+    uint32_t thr, need_eq;
+    radix_select<NT>([&](int64_t c) { return gs.key[c]; }, cnt, static_cast<uint32_t>(k), tid,
+                     sh.hist, sh.warp_sums, &sh.s_bin, &sh.s_above, &thr, &need_eq, sync);
+    uint32_t my_eq = 0;
+    for (uint32_t c = tid; c < cnt; c += NT) {
+        const uint32_t u = gs.key[c];
+        if (u > thr) atomicOr(&gs.bitmap[gs.idx[c] >> 5], 1u << (gs.idx[c] & 31));
+        my_eq += u == thr;
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) my_eq += __shfl_xor_sync(0xFFFFFFFFu, my_eq, o);
+    if (lane == 0 && my_eq) atomicAdd(&gs.n_eq, my_eq);
+    sync();
+    if (gs.n_eq == need_eq) {
+        for (uint32_t c = tid; c < cnt; c += NT)
+            if (gs.key[c] == thr) atomicOr(&gs.bitmap[gs.idx[c] >> 5], 1u << (gs.idx[c] & 31));
+    } else {
+        // more equal keys than kept: the need_eq lowest indices, i.e. the need_eq
+        // largest of ~index among the equal keys (other candidates rank below as 0)
+        uint32_t cut, one;
+        radix_select<NT>(
+            [&](int64_t c) {
+                return gs.key[c] == thr ? ~static_cast<uint32_t>(gs.idx[c]) : 0u;
+            },
+            cnt, need_eq, tid, sh.hist, sh.warp_sums, &sh.s_bin, &sh.s_above, &cut, &one, sync);
+        for (uint32_t c = tid; c < cnt; c += NT)
+            if (gs.key[c] == thr && ~static_cast<uint32_t>(gs.idx[c]) >= cut)
+                atomicOr(&gs.bitmap[gs.idx[c] >> 5], 1u << (gs.idx[c] & 31));
+    }
+    sync();
+    // ---- emission in index order from the bitmap: thread t owns a contiguous run of words
+    const int64_t per = (words + NT - 1) / NT;
+    const int64_t w0 = min(words, per * tid), w1 = min(words, per * (tid + 1));
+    uint32_t mine = 0;
+    for (int64_t w = w0; w < w1; ++w) mine += __popc(gs.bitmap[w]);
+    uint32_t total;
+    uint32_t pos = group_excl_scan<NT>(mine, tid, sh.warp_sums, &total, sync);
+    for (int64_t w = w0; w < w1; ++w) {
+        uint32_t bits = gs.bitmap[w];
+        while (bits) {
+            const int bit = __ffs(bits) - 1;
+            bits &= bits - 1;
+            if (pos < static_cast<uint32_t>(k)) out[pos] = static_cast<int32_t>(32 * w + bit);
+            ++pos;
+        }
+    }
+    return 0;
+}
+
+// Top-k of one score row (L visible scores, L > k) by a group of NT threads with U
+// 16-byte loads in flight per thread: the same algorithm as topk_kernel (2048
+// linear bins between the row's min and max, the threshold bin's scores as
+// candidates, emission of the kept indices in index order). With gs (rows of up to
+// kBits scores) the sample-guided pass runs first and usually ends the row after
+// one pass over it; otherwise, or when it cannot, the plain passes follow.
+template <int NT, int U, int kCap = 1, int kBits = 32, class Sync>
+__device__ void topk_row_vec(const float *__restrict__ src, int64_t L, int32_t k, int32_t nseg,
+                             int32_t *__restrict__ out, TopkShared<NT> &sh, int tid, Sync sync,
+                             GuidedShared<kCap, kBits> *gs = nullptr) {
+    const RowWalk<NT, U> rw(src, L, tid);
+    float vmin, vmax;
+    row_range<NT, U>(rw, nseg, out, sh, tid, sync, &vmin, &vmax);
+    if (vmin == vmax) {
+        // every visible score is equal: the k lowest indices
+        const int warp = tid >> 5;
+        if ((tid & 31) == 0) {
+            sh.w_gt[warp] = 0;
+            sh.w_eq[warp] = static_cast<uint32_t>(rw.hi - rw.lo);
+        }
+        sync();
+        emit_ordered<NT, U>(rw, order_key(vmax), static_cast<uint32_t>(k), out, sh, tid);
+        return;
+    }
+    const LinearBins bin_of{vmin, static_cast<float>(kBins) / (vmax - vmin)};
+    if (gs != nullptr && L <= kBits) {
+        const int r = topk_guided<NT, U>(rw, L, k, bin_of, out, sh, *gs, tid, sync);
+        if (r == 0) return;
+        if (r == 1) {
+            topk_finish<NT, U>(rw, L, k, bin_of, out, sh, tid, sync);
+            return;
+        }
+    }
+    rw.walk([&](int64_t j, const float4 &v) {
+#pragma unroll
+        for (int e = 0; e < 4; ++e)
+            if (j + e < rw.hi) atomicAdd(&sh.hist[bin_of(elem4(v, e))], 1u);
+    }, false);
+    sync();
+    topk_finish<NT, U>(rw, L, k, bin_of, out, sh, tid, sync);
 }
 
 // ------------------------------------------------------------------ score kernel
@@ -932,6 +1129,42 @@ __global__ void __launch_bounds__(NT)
     }
 }
 
+// Long rows with the sample-guided pass: persistent CTAs as topk_vec_kernel, with
+// the guided candidates and the kept-index bitmap in dynamic shared memory.
+constexpr int kGuidedCap = 4096;
+constexpr int kGuidedBits = 262144;  // rows of up to 262,144 scores (1M tokens at ratio 4)
+using LongGuided = GuidedShared<kGuidedCap, kGuidedBits>;
+
+template <int NT, int U>
+constexpr size_t guided_smem() {
+    return sizeof(TopkShared<NT>) + sizeof(LongGuided) + 16;
+}
+
+template <int NT, int U>
+__global__ void __launch_bounds__(NT)
+    topk_guided_kernel(const float *__restrict__ scores, int64_t stride, int64_t n,
+                       int64_t offset, int32_t ratio, int64_t r0, int R, int32_t k,
+                       int32_t nseg, int32_t *__restrict__ sel) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t *base = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 15) & ~static_cast<uintptr_t>(15));
+    TopkShared<NT> &sh = *reinterpret_cast<TopkShared<NT> *>(base);
+    LongGuided *gs = reinterpret_cast<LongGuided *>(base + (sizeof(TopkShared<NT>) + 15) / 16 * 16);
+    for (int it = blockIdx.x; it < R; it += gridDim.x) {
+        const int row = R - 1 - it;
+        const int64_t t = offset + r0 + row;
+        const int64_t L = min(n, (t + 1) / ratio);
+        int32_t *out = sel + (r0 + row) * static_cast<int64_t>(k);
+        if (L <= k) {
+            for (int i = threadIdx.x; i < k; i += NT) out[i] = i < L ? i : -1;
+        } else {
+            topk_row_vec<NT, U>(scores + static_cast<int64_t>(row) * stride, L, k, nseg, out, sh,
+                                threadIdx.x, CtaSync{}, gs);
+        }
+        __syncthreads();  // the shared arrays are reused by the next row
+    }
+}
+
 // Selection without scoring: sel[i, c] = c if c < n_vis(t) else -1 (n = 0: all -1).
 // One CTA per row; 16-byte stores of four entries when k is a multiple of 4.
 __global__ void __launch_bounds__(256) fill_selection_kernel(int32_t *sel, int32_t k,
@@ -1018,10 +1251,16 @@ int launch_topk_tile(const float *scores, int64_t stride, int64_t n, int64_t off
         // rows over 64K scores (256 KB): two persistent 512-thread CTAs per SM with
         // 16-byte loads (a sweep at 1M context: 2 x 512 beat 1 x 1024 per SM, and both
         // beat fewer CTAs that would keep fewer rows in flight; the kernel is bound by
-        // each SM's loads in flight, not by HBM)
+        // each SM's loads in flight, not by HBM). Rows up to kGuidedBits scores take
+        // the sample-guided pass, which usually needs one pass over the row, not three.
         const int grid = static_cast<int>(std::min<int64_t>(R, 2 * sms));
-        topk_vec_kernel<kTopkThreadsLong, 4><<<grid, kTopkThreadsLong, 0, s>>>(
-            scores, stride, n, offset, ratio, r0, static_cast<int>(R), k, nseg_rng, sel);
+        if (n <= kGuidedBits)
+            topk_guided_kernel<kTopkThreadsLong, 4>
+                <<<grid, kTopkThreadsLong, guided_smem<kTopkThreadsLong, 4>(), s>>>(
+                    scores, stride, n, offset, ratio, r0, static_cast<int>(R), k, nseg_rng, sel);
+        else
+            topk_vec_kernel<kTopkThreadsLong, 4><<<grid, kTopkThreadsLong, 0, s>>>(
+                scores, stride, n, offset, ratio, r0, static_cast<int>(R), k, nseg_rng, sel);
     } else if (R < 2 * static_cast<int64_t>(sms)) {
         // few rows (decode steps, short bands): 1024-thread CTAs walk each row faster
         topk_kernel<kTopkThreadsFew><<<static_cast<unsigned>(R), kTopkThreadsFew, 0, s>>>(
@@ -1055,7 +1294,8 @@ int check_score_topk(const void *q_idx, const float *w, const void *pooled_ik, i
 
 namespace {
 
-// Per-device one-time set-up of the score kernel's raised shared-memory limit.
+// Per-device one-time set-up of the raised shared-memory limits (score kernel,
+// sample-guided top-k).
 std::mutex g_score_mu;
 int g_score_setup[kMaxDevices];  // 0 = not yet, else DSA_OK + 1 or the error
 
@@ -1064,9 +1304,13 @@ int score_setup() {
     if (dev < 0) return DSA_ERR_CUDA;
     std::lock_guard<std::mutex> lock(g_score_mu);
     if (g_score_setup[dev] == 0) {
-        const bool ok = cudaFuncSetAttribute(score_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             kScoreSmem) == cudaSuccess;
+        const bool ok =
+            cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kScoreSmem) == cudaSuccess &&
+            cudaFuncSetAttribute(topk_guided_kernel<kTopkThreadsLong, 4>,
+                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(guided_smem<kTopkThreadsLong, 4>())) ==
+                cudaSuccess;
         g_score_setup[dev] = ok ? DSA_OK + 1 : DSA_ERR_CUDA;
     }
     return g_score_setup[dev] == DSA_OK + 1 ? DSA_OK : g_score_setup[dev];

@@ -217,13 +217,15 @@ def test_long_rows_match_oracle(dsa, off, T, k, tile):
 
 @pytest.mark.parametrize("L,m,k,T", [(70000, 30, 64, 320), (70000, 600, 300, 320),
                                      (70000, 1500, 1024, 320), (70000, 100, 3000, 320),
-                                     (70000, 3000, 2048, 96)])
+                                     (70000, 3000, 2048, 96), (70000, 5000, 2048, 96)])
 def test_long_row_topk_heavy_ties_in_tiles(dsa, L, m, k, T):
     """Heavy-tie rows of 70,000 scores through the persistent long-row top-k, in
-    tiles of T/4 rows (each CTA walks several rows): a few candidates ranked against
-    each other, a crowded bin radix-selected, and a bin too crowded to collect
-    (radix select over the row). Checked against the oracle's top-k of the GPU's
-    own scores, exactly, and against a one-tile run."""
+    tiles of T/4 rows (each CTA walks several rows). The sample-guided pass ends
+    most rows; with 600-3000 equal top scores it keeps the lowest indices of the
+    tied ones by a radix select over their indices; with 5000 equal top scores its
+    candidates overflow and the plain passes take over (a bin too crowded to
+    collect: radix select over the row). Checked against the oracle's top-k of the
+    GPU's own scores, exactly, and against a one-tile run."""
     g = torch.Generator().manual_seed(L + m + k + 1)
     off = 4 * L
     n = (off + T) // 4
@@ -253,6 +255,45 @@ def test_long_row_topk_heavy_ties_in_tiles(dsa, L, m, k, T):
     pos = off + np.arange(T)
     assert np.array_equal(sel.cpu().numpy(), oracle.topk(gpu_s, pos, n, 4, k))
     assert torch.equal(sel, sel1)
+
+
+def test_guided_topk_falls_back_when_the_sample_misleads(dsa):
+    """Rows of exactly 70,000 scores whose sampled pieces (17 pieces of 128 scores
+    at 128 * floor(c * 547 / 17), the guided pass's rule for this length) hold
+    the only high scores: the sample places its bin at those scores, but fewer of
+    them exist than index_topk, so the k-th largest lies below it and the plain
+    passes must finish the row. Every score is a monotone function of one key
+    coefficient, so the expected selection is known exactly."""
+    L, k, T = 70000, 3000, 4
+    off = 4 * L - 1                      # rows t = off..off+3 all see L pooled rows
+    n = (off + T) // 4
+    assert n == L and all((off + i + 1) // 4 == L for i in range(T))
+    g = torch.Generator().manual_seed(70)
+    v = torch.randn(128, generator=g)
+    unit = v / v.norm()
+    alpha = torch.rand(n, generator=g) * 2.0 - 1.0
+    pieces, ns = (L + 127) // 128, max(8, min(64, L // 4096))
+    for c in range(ns):
+        b = (c * pieces // ns) * 128
+        alpha[b:b + 128] = 2.0 + 0.001 * torch.arange(128)   # the high scores
+    pik = (alpha[:, None] * unit[None, :] * 4.0).to(torch.bfloat16)
+    q_idx = v.expand(T, 64, 128).to(torch.bfloat16).contiguous()
+    w = torch.rand(T, 64, generator=g) * 0.125 + 0.01
+    sel = torch.empty(T, k, dtype=torch.int32, device="cuda")
+    scratch = torch.empty(B.dsa_score_scratch_bytes(T, n) // 4, dtype=torch.float32,
+                          device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.dsa_index_score_topk(q_idx.cuda(), w.cuda(), pik.cuda(), n, T, off, 4, k, T, scratch,
+                           sel, status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    stride = (n + 127) // 128 * 128
+    gpu_s = scratch[: T * stride].view(T, stride)[:, :n].cpu().numpy()
+    high = np.isin(np.arange(n), np.concatenate(
+        [np.arange((c * pieces // ns) * 128, (c * pieces // ns) * 128 + 128) for c in range(ns)]))
+    assert high.sum() < k and (gpu_s[:, high].min(axis=1) > gpu_s[:, ~high].max(axis=1)).all()
+    pos = off + np.arange(T)
+    assert np.array_equal(sel.cpu().numpy(), oracle.topk(gpu_s, pos, n, 4, k))
 
 
 @pytest.mark.parametrize("tiles", [(1, 7, 64, 333), (512, 1000)])
