@@ -63,7 +63,6 @@ namespace {
 // empty for a moment. With two, one warp's waits are covered by the other's
 // queued MMAs.
 constexpr int kLoadWarps = 6;
-constexpr int kMaxGroups = (32 + kLoadWarps - 1) / kLoadWarps;  // 4-row groups per loader warp
 constexpr int kQkWarp = 6;
 constexpr int kPvWarp = 7;
 constexpr int kSoftWarp0 = 8;
@@ -156,22 +155,6 @@ __device__ __forceinline__ void bar_group(int hh) {
 }
 
 __device__ __forceinline__ void bar_soft() { asm volatile("bar.sync 3, 256;" ::: "memory"); }
-
-// A 16-byte global load issued where it stands: volatile, so the compiler neither
-// moves it nor re-issues it later in place of keeping its registers.
-__device__ __forceinline__ uint4 ld_keep16(const void *src) {
-    uint4 v;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
-                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
-                 : "l"(src));
-    return v;
-}
-
-__device__ __forceinline__ void st_shared16(uint32_t dst, const uint4 &v) {
-    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(dst), "r"(v.x), "r"(v.y),
-                 "r"(v.z), "r"(v.w)
-                 : "memory");
-}
 
 __device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
@@ -394,38 +377,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 cp_async_arrive(&x_full[par]);
                 jn = (b + kSplit < x.nb) ? fetch(x, i, b + kSplit)
                                          : (inext < p.T ? fetch(xnext, inext, crank) : -1);
-                // chunk 6 is the last slot the previous block's PV releases: its rows are
-                // read into registers now, so that once the slot is free only the
-                // shared-memory stores stand between the release and this block's last QK
-                uint4 c6[kMaxGroups];
-#pragma unroll
-                for (int gq = 0; gq < kMaxGroups; ++gq) {
-                    if (gq < ngroups) {
-                        const int srow = __shfl_sync(0xFFFFFFFFu, row, 4 * gq + a);
-                        c6[gq] = ld_keep16(
-                            src_base + static_cast<int64_t>(srow) * (kD * 2) + 6 * 128);
-                    }
-                }
-                // chunk pairs 0-2 by cp.async, then chunk 6 from the registers, as the
-                // previous block's PV releases them
+                // chunk pairs 0-2, then chunk 6, as the previous block's PV releases them
                 for (int m = 0; m < 4 && ok; ++m) {
                     if (lane == 0) ok = mbar_wait(&kv_free[m], (g & 1) ^ 1, abort_flag, p.status);
                     ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
                     if (!ok) break;
-                    if (m == 3) {
-#pragma unroll
-                        for (int gq = 0; gq < kMaxGroups; ++gq) {
-                            if (gq < ngroups) {
-                                const int r = 4 * (lw + kLoadWarps * gq) + a;
-                                st_shared16(kv_base + r * 128 + ((pc ^ (r & 7)) << 4) + 6 * 16384,
-                                            c6[gq]);
-                            }
-                        }
-                        // generic-proxy stores, read next by the MMA's async proxy
-                        fence_proxy_async_smem();
-                        mbar_arrive(&kv_full[3]);
-                        break;
-                    }
 #pragma unroll 1
                     for (int gq = 0; gq < ngroups; ++gq) {
                         const int r = 4 * (lw + kLoadWarps * gq) + a;
@@ -433,7 +389,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         const uint8_t *src = src_base + static_cast<int64_t>(srow) * (kD * 2);
                         const uint32_t dst = kv_base + r * 128 + ((pc ^ (r & 7)) << 4);
                         cp_async16(dst + (2 * m) * 16384, src + (2 * m) * 128);
-                        cp_async16(dst + (2 * m + 1) * 16384, src + (2 * m + 1) * 128);
+                        if (m < 3) cp_async16(dst + (2 * m + 1) * 16384, src + (2 * m + 1) * 128);
                     }
                     cp_async_arrive(&kv_full[m]);
                 }

@@ -1129,18 +1129,15 @@ __global__ void __launch_bounds__(NT)
     }
 }
 
-// Long rows with the sample-guided pass: persistent CTAs as topk_vec_kernel, with
-// the guided candidates and the kept-index bitmap in dynamic shared memory.
-constexpr int kGuidedCap = 4096;
-constexpr int kGuidedBits = 262144;  // rows of up to 262,144 scores (1M tokens at ratio 4)
-using LongGuided = GuidedShared<kGuidedCap, kGuidedBits>;
-
-template <int NT, int U>
+// The sample-guided pass in persistent CTAs (as topk_vec_kernel), with its
+// candidates and kept-index bitmap in dynamic shared memory: rows of up to kBits
+// scores, up to kCap candidates.
+template <int NT, int U, int kCap, int kBits>
 constexpr size_t guided_smem() {
-    return sizeof(TopkShared<NT>) + sizeof(LongGuided) + 16;
+    return (sizeof(TopkShared<NT>) + 15) / 16 * 16 + sizeof(GuidedShared<kCap, kBits>) + 16;
 }
 
-template <int NT, int U>
+template <int NT, int U, int kCap, int kBits>
 __global__ void __launch_bounds__(NT)
     topk_guided_kernel(const float *__restrict__ scores, int64_t stride, int64_t n,
                        int64_t offset, int32_t ratio, int64_t r0, int R, int32_t k,
@@ -1149,7 +1146,8 @@ __global__ void __launch_bounds__(NT)
     uint8_t *base = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 15) & ~static_cast<uintptr_t>(15));
     TopkShared<NT> &sh = *reinterpret_cast<TopkShared<NT> *>(base);
-    LongGuided *gs = reinterpret_cast<LongGuided *>(base + (sizeof(TopkShared<NT>) + 15) / 16 * 16);
+    auto *gs = reinterpret_cast<GuidedShared<kCap, kBits> *>(
+        base + (sizeof(TopkShared<NT>) + 15) / 16 * 16);
     for (int it = blockIdx.x; it < R; it += gridDim.x) {
         const int row = R - 1 - it;
         const int64_t t = offset + r0 + row;
@@ -1164,6 +1162,16 @@ __global__ void __launch_bounds__(NT)
         __syncthreads();  // the shared arrays are reused by the next row
     }
 }
+
+// Rows of up to 262,144 scores (1M tokens at ratio 4), 4096 candidates: 512-thread
+// CTAs, two per SM. Rows of up to 65,536 scores: 256-thread CTAs, three per SM.
+constexpr int kGuidedCap = 4096;
+constexpr int kLongBits = 262144;
+constexpr int kShortBits = 65536;
+#define DSA_GUIDED_LONG topk_guided_kernel<kTopkThreadsLong, 4, kGuidedCap, kLongBits>
+#define DSA_GUIDED_SHORT topk_guided_kernel<kTopkThreads, 4, kGuidedCap, kShortBits>
+constexpr size_t kGuidedLongSmem = guided_smem<kTopkThreadsLong, 4, kGuidedCap, kLongBits>();
+constexpr size_t kGuidedShortSmem = guided_smem<kTopkThreads, 4, kGuidedCap, kShortBits>();
 
 // Selection without scoring: sel[i, c] = c if c < n_vis(t) else -1 (n = 0: all -1).
 // One CTA per row; 16-byte stores of four entries when k is a multiple of 4.
@@ -1251,13 +1259,12 @@ int launch_topk_tile(const float *scores, int64_t stride, int64_t n, int64_t off
         // rows over 64K scores (256 KB): two persistent 512-thread CTAs per SM with
         // 16-byte loads (a sweep at 1M context: 2 x 512 beat 1 x 1024 per SM, and both
         // beat fewer CTAs that would keep fewer rows in flight; the kernel is bound by
-        // each SM's loads in flight, not by HBM). Rows up to kGuidedBits scores take
-        // the sample-guided pass, which usually needs one pass over the row, not three.
+        // each SM's loads in flight, not by HBM). Rows up to kLongBits scores take the
+        // sample-guided pass, which usually needs one pass over the row, not three.
         const int grid = static_cast<int>(std::min<int64_t>(R, 2 * sms));
-        if (n <= kGuidedBits)
-            topk_guided_kernel<kTopkThreadsLong, 4>
-                <<<grid, kTopkThreadsLong, guided_smem<kTopkThreadsLong, 4>(), s>>>(
-                    scores, stride, n, offset, ratio, r0, static_cast<int>(R), k, nseg_rng, sel);
+        if (n <= kLongBits)
+            DSA_GUIDED_LONG<<<grid, kTopkThreadsLong, kGuidedLongSmem, s>>>(
+                scores, stride, n, offset, ratio, r0, static_cast<int>(R), k, nseg_rng, sel);
         else
             topk_vec_kernel<kTopkThreadsLong, 4><<<grid, kTopkThreadsLong, 0, s>>>(
                 scores, stride, n, offset, ratio, r0, static_cast<int>(R), k, nseg_rng, sel);
@@ -1307,10 +1314,10 @@ int score_setup() {
         const bool ok =
             cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kScoreSmem) == cudaSuccess &&
-            cudaFuncSetAttribute(topk_guided_kernel<kTopkThreadsLong, 4>,
-                                 cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(guided_smem<kTopkThreadsLong, 4>())) ==
-                cudaSuccess;
+            cudaFuncSetAttribute(DSA_GUIDED_LONG, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kGuidedLongSmem)) == cudaSuccess &&
+            cudaFuncSetAttribute(DSA_GUIDED_SHORT, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kGuidedShortSmem)) == cudaSuccess;
         g_score_setup[dev] = ok ? DSA_OK + 1 : DSA_ERR_CUDA;
     }
     return g_score_setup[dev] == DSA_OK + 1 ? DSA_OK : g_score_setup[dev];
