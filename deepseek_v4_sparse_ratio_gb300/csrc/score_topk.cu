@@ -1164,14 +1164,13 @@ __global__ void __launch_bounds__(NT)
 }
 
 // Rows of up to 262,144 scores (1M tokens at ratio 4), 4096 candidates: 512-thread
-// CTAs, two per SM. Rows of up to 65,536 scores: 256-thread CTAs, three per SM.
+// CTAs, two per SM. (For rows of up to 64K scores, which stay in L2 across the
+// passes, the one-row-per-CTA kernel measured faster: 1.77 against 1.84-2.01 ms
+// for score + top-k at 128K context.)
 constexpr int kGuidedCap = 4096;
 constexpr int kLongBits = 262144;
-constexpr int kShortBits = 65536;
 #define DSA_GUIDED_LONG topk_guided_kernel<kTopkThreadsLong, 4, kGuidedCap, kLongBits>
-#define DSA_GUIDED_SHORT topk_guided_kernel<kTopkThreads, 4, kGuidedCap, kShortBits>
 constexpr size_t kGuidedLongSmem = guided_smem<kTopkThreadsLong, 4, kGuidedCap, kLongBits>();
-constexpr size_t kGuidedShortSmem = guided_smem<kTopkThreads, 4, kGuidedCap, kShortBits>();
 
 // Selection without scoring: sel[i, c] = c if c < n_vis(t) else -1 (n = 0: all -1).
 // One CTA per row; 16-byte stores of four entries when k is a multiple of 4.
@@ -1315,9 +1314,7 @@ int score_setup() {
             cudaFuncSetAttribute(score_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kScoreSmem) == cudaSuccess &&
             cudaFuncSetAttribute(DSA_GUIDED_LONG, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kGuidedLongSmem)) == cudaSuccess &&
-            cudaFuncSetAttribute(DSA_GUIDED_SHORT, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kGuidedShortSmem)) == cudaSuccess;
+                                 static_cast<int>(kGuidedLongSmem)) == cudaSuccess;
         g_score_setup[dev] = ok ? DSA_OK + 1 : DSA_ERR_CUDA;
     }
     return g_score_setup[dev] == DSA_OK + 1 ? DSA_OK : g_score_setup[dev];
