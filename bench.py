@@ -96,13 +96,13 @@ def score_scratch_bytes(wl, tile):
 # the sources the captured build came from; a changed source reports null.
 NCU_TRAFFIC = {
     "attn_kernel": {"bytes": 343.090e6 + 233.841e6, "files": ("attn.cu", "common.cuh", "internal.h"),
-                    "sha256_16": "fe0dab3904f249fd"},
+                    "sha256_16": "2e588b224f0a2709"},
     "score_kernel": {"bytes": 76.969e6 + 476.884e6,
                      "files": ("score_topk.cu", "common.cuh", "internal.h"),
-                     "sha256_16": "f57a76f06175089d"},
+                     "sha256_16": "51dd0570c634929a"},
     "topk_kernel": {"bytes": 692.426e6 + 30.576e6,
                     "files": ("score_topk.cu", "common.cuh", "internal.h"),
-                    "sha256_16": "f57a76f06175089d"},
+                    "sha256_16": "51dd0570c634929a"},
 }
 
 

@@ -1,5 +1,5 @@
 // Shared device helpers for the sm_103a kernels: mbarriers with bounded waits,
-// TMA tile/gather loads, tcgen05 (TMEM allocation, MMA, loads) and the
+// TMA tile loads, tcgen05 (TMEM allocation, MMA, loads) and the
 // shared-memory matrix descriptors the MMA reads its operands through.
 #pragma once
 
@@ -99,17 +99,6 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *tm, ui
         "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
         " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_u32(dst)),
         "l"(tm), "r"(x), "r"(y), "r"(smem_u32(bar)), "l"(policy)
-        : "memory");
-}
-
-// Gather of four rows y0..y3 (box one row high, x elements wide) into four
-// consecutive box rows of shared memory.
-__device__ __forceinline__ void tma_gather4(void *dst, const CUtensorMap *tm, uint64_t *bar, int x,
-                                            int y0, int y1, int y2, int y3, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cta.global.tile::gather4.mbarrier::complete_tx::bytes"
-        ".L2::cache_hint [%0], [%1, {%2, %3, %4, %5, %6}], [%7], %8;" ::"r"(smem_u32(dst)),
-        "l"(tm), "r"(x), "r"(y0), "r"(y1), "r"(y2), "r"(y3), "r"(smem_u32(bar)), "l"(policy)
         : "memory");
 }
 
