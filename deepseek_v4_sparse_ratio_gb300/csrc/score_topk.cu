@@ -54,6 +54,7 @@ namespace {
 
 constexpr int kBins = 2048;
 constexpr int kCandCap = 2048;
+constexpr uint32_t kNoBin = 0xFFFFFFFFu;  // find_bin found no bin (fewer than `need` counted)
 
 __device__ __forceinline__ uint32_t order_key(float f) {
     const uint32_t b = __float_as_uint(f);
@@ -424,14 +425,15 @@ struct GuidedShared {
 //     row, gives a bin tau that lies, with a wide margin, below the bin of the k-th
 //     largest score (the sample's rank k * samples / L plus 3 standard deviations
 //     plus 8);
-//  2. one pass over the row builds the full histogram and collects every score in
-//     bins >= tau (key, index);
+//  2. one pass over the row counts and collects every score in bins >= tau (key,
+//     index); the bins below tau are not counted, so most scores cost a compare;
 //  3. if the k-th largest lies in a bin >= tau and the candidates fit, it and its
 //     kept equals are found exactly among the candidates (radix select); the kept
 //     indices are set in a bitmap (ties at the threshold: the lowest indices) and
 //     emitted in index order from it, without another pass over the scores.
 // Returns 0 when the row is done; 1 when step 3 does not apply (sh.hist then holds
-// the row's full histogram); 2 when the sample cannot place tau (sh.hist zeroed).
+// the row's full histogram, built by one more pass); 2 when the sample cannot place
+// tau (sh.hist zeroed).
 template <int NT, int U, int kCap, int kBits, class Sync>
 __device__ int topk_guided(const RowWalk<NT, U> &rw, int64_t L, int32_t k, LinearBins bin_of,
                            int32_t *__restrict__ out, TopkShared<NT> &sh,
@@ -474,14 +476,16 @@ __device__ int topk_guided(const RowWalk<NT, U> &rw, int64_t L, int32_t k, Linea
     for (int i = tid; i < kBins; i += NT) sh.hist[i] = 0;
     sync();
     if (tau < 0) return 2;
-    // ---- 2. full histogram, candidates of bins >= tau
+    // ---- 2. the histogram of bins >= tau (only those can hold the k-th largest score if
+    // the sample was right, and the bins below are never read then), candidates of the
+    // same bins
     rw.walk([&](int64_t j, const float4 &v) {
 #pragma unroll
         for (int e = 0; e < 4; ++e)
             if (j + e < rw.hi) {
                 const int b = bin_of(elem4(v, e));
-                atomicAdd(&sh.hist[b], 1u);
                 if (b >= tau) {
+                    atomicAdd(&sh.hist[b], 1u);
                     const uint32_t c = atomicAdd(&gs.cnt, 1u);
                     if (c < kCap) {
                         gs.key[c] = order_key(elem4(v, e));
@@ -490,11 +494,24 @@ __device__ int topk_guided(const RowWalk<NT, U> &rw, int64_t L, int32_t k, Linea
                 }
             }
     }, false);
+    if (tid == 0) sh.s_bin = kNoBin;  // stays if the bins >= tau hold fewer than k scores
     sync();
     find_bin<NT>(sh.hist, kBins, static_cast<uint32_t>(k), tid, sh.warp_sums, &sh.s_bin,
                  &sh.s_above, sync);
     const uint32_t cnt = gs.cnt;
-    if (static_cast<int>(sh.s_bin) < tau || cnt > static_cast<uint32_t>(kCap)) return 1;
+    if (sh.s_bin == kNoBin || cnt > static_cast<uint32_t>(kCap)) {
+        // the sample misled (the k-th largest lies below tau) or the candidates overflow:
+        // the full histogram for the plain passes
+        for (int i = tid; i < kBins; i += NT) sh.hist[i] = 0;
+        sync();
+        rw.walk([&](int64_t j, const float4 &v) {
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+                if (j + e < rw.hi) atomicAdd(&sh.hist[bin_of(elem4(v, e))], 1u);
+        }, false);
+        sync();
+        return 1;
+    }
     // ---- 3. every score of the bins >= tau is a candidate, so the k-th largest score
     // overall is the k-th largest candidate
     uint32_t thr, need_eq;
