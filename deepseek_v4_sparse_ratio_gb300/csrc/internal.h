@@ -67,9 +67,12 @@ int check_score_topk(const void *q_idx, const float *w, const void *pooled_ik, i
                      const void *scratch, size_t scratch_bytes, const int32_t *sel);
 int prepare_score_topk(const void *q_idx, const void *pooled_ik, int64_t n, int64_t chunk,
                        int32_t k, ScoreTopkPlan *plan);
-int enqueue_score_topk(const ScoreTopkPlan &plan, const float *w, int64_t n, int64_t chunk,
-                       int64_t offset, int32_t ratio, int32_t k, int64_t tile_rows,
-                       void *scratch, int32_t *sel, int32_t *status, cudaStream_t s);
+// Rows [r_begin, r_end) of the chunk, in tiles of at most tile_rows rows (each tile's
+// scores start at the scratch's first row); `plan` covers the whole chunk.
+int enqueue_score_topk(const ScoreTopkPlan &plan, const float *w, int64_t n, int64_t offset,
+                       int32_t ratio, int32_t k, int64_t r_begin, int64_t r_end,
+                       int64_t tile_rows, void *scratch, int32_t *sel, int32_t *status,
+                       cudaStream_t s);
 
 // Window + selected attention (step d).
 struct AttnPlan {

@@ -61,8 +61,8 @@ int enqueue_pool_and_select(const dsa_pool_state *st, const ScoreTopkPlan &plan,
         static_cast<const uint8_t *>(raw_kv) + (offset - raw_start) * int64_t{kD} * 2;
     int rc = launch_pool_append(*st, chunk_kv, raw_ik, chunk, offset, s);
     if (rc != DSA_OK) return rc;
-    return enqueue_score_topk(plan, w, n, chunk, offset, ratio, index_topk, tile_rows, scratch,
-                              sel, status, s);
+    return enqueue_score_topk(plan, w, n, offset, ratio, index_topk, 0, chunk, tile_rows,
+                              scratch, sel, status, s);
 }
 
 }  // namespace
@@ -100,13 +100,14 @@ extern "C" int dsa_prefill_chunk(dsa_pool_state *st, const void *raw_kv, int64_t
 namespace {
 
 struct Events {
-    cudaEvent_t e[12] = {};
+    static constexpr int kMax = 16;
+    cudaEvent_t e[kMax] = {};
     int n = 0;
     ~Events() {
         for (int i = 0; i < n; ++i) cudaEventDestroy(e[i]);  // released once complete
     }
     cudaEvent_t make() {
-        if (n == 12 || cudaEventCreateWithFlags(&e[n], cudaEventDisableTiming) != cudaSuccess)
+        if (n == kMax || cudaEventCreateWithFlags(&e[n], cudaEventDisableTiming) != cudaSuccess)
             return nullptr;
         return e[n++];
     }
@@ -132,19 +133,39 @@ extern "C" int dsa_prefill_chunk_host(dsa_pool_state *st, const dsa_prefill_work
     if (rc != DSA_OK) return rc;
     const int64_t end = offset + chunk;
     const int64_t n = end / st->ratio;
-    const size_t q_row = size_t{kH} * kD * 2;  // bytes of one query row (all heads)
+    const size_t q_row = size_t{kH} * kD * 2;    // bytes of one query row (all heads)
+    const size_t qi_row = size_t{kHI} * kDI * 2; // bytes of one indexer query row
+    const size_t sel_row = size_t(index_topk) * 4;
+    const int64_t sms = sm_count() > 0 ? sm_count() : 1;
+
+    // every step's plan (tensor maps, per-device set-up), before the first copy or launch
+    ScoreTopkPlan splan;
+    rc = prepare_score_topk(ws->q_idx, st->pooled_ik, n, chunk, index_topk, &splan);
+    if (rc != DSA_OK) return rc;
+
+    // The indexer queries are the largest input the scoring waits for. The first score
+    // tile is short (an eighth of the chunk), so it starts once its own rows have landed
+    // while the rest copy on the other stream; the rows after it follow in tiles of
+    // tile_rows. Results do not depend on the tiling. (At 4096 rows and 128K context a
+    // first tile of 512 rows measured 3.82 ms end to end, 768 rows 3.85, 1024 rows 3.88,
+    // 1536 rows 3.92.)
+    int64_t first = std::min(tile_rows, chunk);
+    if (splan.full && chunk >= 1024)
+        first = std::min(first, std::max<int64_t>(256, (chunk / 8 + 127) / 128 * 128));
 
     // attention in row slices; each slice's output goes back while the next computes.
-    // Slices shrink towards the end (whole waves of one row per SM where possible), so
-    // the copy left exposed after the last kernel is short: the output copy of a slice
-    // takes about 0.75 of the kernel time of a slice of the same size, so each slice
-    // may be about 0.75 of the one before it.
+    // The output copy of a row takes about 0.83 of the kernel time of a row, so the
+    // slices shrink towards the end by about that factor (whole waves of one row per
+    // SM where possible): the copy left exposed after the last kernel is short and no
+    // copy backlog builds up; the first slice is short enough that the output copies
+    // start soon after the selection's. (At 4096 rows and 128K context these seven
+    // slices measured 3.88 ms end to end against 3.98 for five slices of 30, 26, 22, 14
+    // and 8 % of the rows, with the same first score tile.)
     int64_t cuts[8];
     int ncut = 0;
     {
-        const int64_t sms = sm_count() > 0 ? sm_count() : 1;
         const int64_t waves = (chunk + sms - 1) / sms;
-        static const double kCum[] = {0.30, 0.56, 0.78, 0.92};
+        static const double kCum[] = {0.22, 0.41, 0.59, 0.74, 0.85, 0.93};
         if (chunk >= 1024) {
             for (double f : kCum) {
                 const int64_t r = static_cast<int64_t>(f * static_cast<double>(waves) + 0.5) * sms;
@@ -153,11 +174,7 @@ extern "C" int dsa_prefill_chunk_host(dsa_pool_state *st, const dsa_prefill_work
         }
         cuts[ncut++] = chunk;
     }
-    // every step's plan (tensor maps, per-device set-up) and every event, before the
-    // first copy or launch
-    ScoreTopkPlan splan;
     AttnPlan aplan[8];
-    rc = prepare_score_topk(ws->q_idx, st->pooled_ik, n, chunk, index_topk, &splan);
     for (int ci = 0; ci < ncut && rc == DSA_OK; ++ci) {
         const int64_t r0 = ci ? cuts[ci - 1] : 0;
         rc = prepare_attention(static_cast<const uint8_t *>(ws->q) + r0 * q_row, cuts[ci] - r0,
@@ -165,35 +182,59 @@ extern "C" int dsa_prefill_chunk_host(dsa_pool_state *st, const dsa_prefill_work
     }
     if (rc != DSA_OK) return rc;
     Events ev;
-    cudaEvent_t in_done = ev.make(), q_done = ev.make(), sel_done = ev.make(), all_done = ev.make();
+    cudaEvent_t in_done = ev.make(), qi_done = ev.make(), q_done = ev.make(),
+                sel0_done = ev.make(), sel_done = ev.make(), all_done = ev.make();
     cudaEvent_t slice_done[8] = {};
-    bool have_events = in_done && q_done && sel_done && all_done;
+    bool have_events = in_done && qi_done && q_done && sel0_done && sel_done && all_done;
     for (int ci = 0; ci < ncut; ++ci) have_events = have_events && (slice_done[ci] = ev.make());
     if (!have_events) return DSA_ERR_CUDA;
 
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     cudaStream_t c = static_cast<cudaStream_t>(copy_stream);
     const cudaMemcpyKind h2d = cudaMemcpyHostToDevice, d2h = cudaMemcpyDeviceToHost;
+    const uint8_t *q_idx_hb = static_cast<const uint8_t *>(q_idx_h);
+    uint8_t *q_idx_db = static_cast<uint8_t *>(ws->q_idx);
+    uint8_t *sel_hb = reinterpret_cast<uint8_t *>(sel_h);
+    const uint8_t *sel_db = reinterpret_cast<const uint8_t *>(ws->sel);
     bool ok = true;
-    // inputs of pooling and the indexer on the compute stream; the query rows follow on
-    // the copy stream and land while pooling and the indexer run
+    // inputs of pooling and the first score tile on the compute stream; the other
+    // indexer query rows, then the attention queries, on the copy stream, landing while
+    // pooling and the indexer run
     ok = ok && cudaMemcpyAsync(ws->raw_kv, raw_kv_h, size_t(raw_rows) * kD * 2, h2d, s) == cudaSuccess;
     ok = ok && cudaMemcpyAsync(ws->raw_ik, raw_ik_h, size_t(chunk) * kDI * 2, h2d, s) == cudaSuccess;
-    ok = ok && cudaMemcpyAsync(ws->q_idx, q_idx_h, size_t(chunk) * kHI * kDI * 2, h2d, s) == cudaSuccess;
     ok = ok && cudaMemcpyAsync(ws->w, w_h, size_t(chunk) * kHI * 4, h2d, s) == cudaSuccess;
+    ok = ok && cudaMemcpyAsync(q_idx_db, q_idx_hb, size_t(first) * qi_row, h2d, s) == cudaSuccess;
     ok = ok && cudaEventRecord(in_done, s) == cudaSuccess;
     ok = ok && cudaStreamWaitEvent(c, in_done, 0) == cudaSuccess;
+    if (first < chunk)
+        ok = ok && cudaMemcpyAsync(q_idx_db + first * qi_row, q_idx_hb + first * qi_row,
+                                   size_t(chunk - first) * qi_row, h2d, c) == cudaSuccess;
+    ok = ok && cudaEventRecord(qi_done, c) == cudaSuccess;
     ok = ok && cudaMemcpyAsync(ws->q, q_h, size_t(chunk) * q_row, h2d, c) == cudaSuccess;
     ok = ok && cudaEventRecord(q_done, c) == cudaSuccess;
     if (!ok) return DSA_ERR_CUDA;
 
-    rc = enqueue_pool_and_select(st, splan, ws->raw_kv, raw_start, ws->raw_ik, ws->w, chunk,
-                                 offset, index_topk, tile_rows, ws->scratch, ws->sel,
-                                 dev_status, s);
+    const void *chunk_kv =
+        static_cast<const uint8_t *>(ws->raw_kv) + (offset - raw_start) * int64_t{kD} * 2;
+    rc = launch_pool_append(*st, chunk_kv, ws->raw_ik, chunk, offset, s);
+    if (rc == DSA_OK)
+        rc = enqueue_score_topk(splan, ws->w, n, offset, st->ratio, index_topk, 0, first,
+                                tile_rows, ws->scratch, ws->sel, dev_status, s);
+    if (rc != DSA_OK) return rc;
+    ok = ok && cudaEventRecord(sel0_done, s) == cudaSuccess;
+    ok = ok && cudaStreamWaitEvent(s, qi_done, 0) == cudaSuccess;
+    if (!ok) return DSA_ERR_CUDA;
+    rc = enqueue_score_topk(splan, ws->w, n, offset, st->ratio, index_topk, first, chunk,
+                            tile_rows, ws->scratch, ws->sel, dev_status, s);
     if (rc != DSA_OK) return rc;
     ok = ok && cudaEventRecord(sel_done, s) == cudaSuccess;
+    // the selection goes back in two parts, the first while the later tiles score
+    ok = ok && cudaStreamWaitEvent(c, sel0_done, 0) == cudaSuccess;
+    ok = ok && cudaMemcpyAsync(sel_hb, sel_db, size_t(first) * sel_row, d2h, c) == cudaSuccess;
     ok = ok && cudaStreamWaitEvent(c, sel_done, 0) == cudaSuccess;
-    ok = ok && cudaMemcpyAsync(sel_h, ws->sel, size_t(chunk) * index_topk * 4, d2h, c) == cudaSuccess;
+    if (first < chunk)
+        ok = ok && cudaMemcpyAsync(sel_hb + first * sel_row, sel_db + first * sel_row,
+                                   size_t(chunk - first) * sel_row, d2h, c) == cudaSuccess;
     ok = ok && cudaStreamWaitEvent(s, q_done, 0) == cudaSuccess;
     if (!ok) return DSA_ERR_CUDA;
 

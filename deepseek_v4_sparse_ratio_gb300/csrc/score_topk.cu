@@ -1353,14 +1353,18 @@ int prepare_score_topk(const void *q_idx, const void *pooled_ik, int64_t n, int6
     return DSA_OK;
 }
 
-int enqueue_score_topk(const ScoreTopkPlan &plan, const float *w, int64_t n, int64_t chunk,
-                       int64_t offset, int32_t ratio, int32_t k, int64_t tile_rows,
-                       void *scratch, int32_t *sel, int32_t *status, cudaStream_t s) {
-    if (!plan.full) return launch_fill_selection(sel, chunk, k, offset, n, ratio, s);
+int enqueue_score_topk(const ScoreTopkPlan &plan, const float *w, int64_t n, int64_t offset,
+                       int32_t ratio, int32_t k, int64_t r_begin, int64_t r_end,
+                       int64_t tile_rows, void *scratch, int32_t *sel, int32_t *status,
+                       cudaStream_t s) {
+    if (r_end <= r_begin) return DSA_OK;
+    if (!plan.full)
+        return launch_fill_selection(sel + r_begin * k, r_end - r_begin, k, offset + r_begin, n,
+                                     ratio, s);
     const int64_t stride = score_stride(n);
     float *scores = static_cast<float *>(scratch);
-    for (int64_t r0 = 0; r0 < chunk; r0 += tile_rows) {
-        const int64_t R = std::min(tile_rows, chunk - r0);
+    for (int64_t r0 = r_begin; r0 < r_end; r0 += tile_rows) {
+        const int64_t R = std::min(tile_rows, r_end - r0);
         int nseg_rng = 0;
         int rc = launch_score_tile(plan.tm_q, plan.tm_k, w, n, offset, ratio, r0, R, scores,
                                    stride, sel, k, &nseg_rng, status, s);
@@ -1391,7 +1395,7 @@ extern "C" int dsa_index_score_topk(const void *q_idx, const float *w, const voi
     ScoreTopkPlan plan;
     rc = prepare_score_topk(q_idx, pooled_ik, n_pooled, chunk, index_topk, &plan);
     if (rc != DSA_OK) return rc;
-    return enqueue_score_topk(plan, w, n_pooled, chunk, offset, ratio, index_topk, tile_rows,
+    return enqueue_score_topk(plan, w, n_pooled, offset, ratio, index_topk, 0, chunk, tile_rows,
                               scratch, sel, dev_status, static_cast<cudaStream_t>(stream));
 }
 
@@ -1482,6 +1486,6 @@ extern "C" int dsa_index_score_topk_noalloc(const void *q_idx, const float *w,
     ScoreTopkPlan plan;
     rc = prepare_score_topk(q_idx, pooled_ik, n_pooled, chunk, index_topk, &plan);
     if (rc != DSA_OK) return rc;
-    return enqueue_score_topk(plan, w, n_pooled, chunk, offset, ratio, index_topk, tile_rows,
+    return enqueue_score_topk(plan, w, n_pooled, offset, ratio, index_topk, 0, chunk, tile_rows,
                               scratch, sel, dev_status, static_cast<cudaStream_t>(stream));
 }

@@ -265,11 +265,14 @@ typedef struct dsa_prefill_workspace {
  *   raw_rows <= ws->raw_kv_rows, ws->scratch as for dsa_prefill_chunk.
  *   stream: the compute stream; copy_stream: a second stream for the copies
  *   that overlap compute (the query copy, the selection and output copies), or
- *   the same stream to serialize everything. Ordering: the inputs are copied
- *   on `stream`, the query rows on copy_stream while the pooling and indexer
- *   run, the attention runs in up to five row slices of shrinking size and
- *   each slice's output is copied back on copy_stream while the next slice
- *   computes. When `stream`
+ *   the same stream to serialize everything. Ordering: the inputs of pooling
+ *   and of the first score tile (the chunk's first eighth of the indexer query
+ *   rows) are copied on `stream`, the other indexer query rows and then the
+ *   query rows on copy_stream while the pooling and indexer run; the later
+ *   score tiles wait for their rows; the selection of the first tile is copied
+ *   back while the later tiles score; the attention runs in up to seven row
+ *   slices of shrinking size and each slice's output is copied back on
+ *   copy_stream while the next slice computes. When `stream`
  *   completes, every copy has completed and the host outputs are valid.
  *   The host buffers must stay alive and unmodified until then.
  * Errors: those of dsa_prefill_chunk; DSA_ERR_ARG for a null host pointer or
