@@ -28,12 +28,18 @@ def _small(kind):
     return inputs.workload(kind)
 
 
-@pytest.mark.parametrize("name,copy_stream", [("two_chunks_4098", True),
-                                              ("two_chunks_4098", False),
-                                              ("skip_then_full", True),
-                                              ("decode", True)])
-def test_host_path_equals_device_path(dsa, name, copy_stream):
+# The host path scores a short first tile (an eighth of a chunk of 1024 rows or more, at
+# most tile_rows) before the rest, in tiles of tile_rows: a tile of 200 rows makes the
+# first tile and every later one start off a multiple of the tile size.
+@pytest.mark.parametrize("name,copy_stream,tile", [("two_chunks_4098", True, None),
+                                                   ("two_chunks_4098", False, None),
+                                                   ("two_chunks_4098", True, 200),
+                                                   ("skip_then_full", True, None),
+                                                   ("decode", True, None)])
+def test_host_path_equals_device_path(dsa, name, copy_stream, tile):
     wl = inputs.draw(_small(name))
+    if tile:
+        wl.tile_rows = (tile,)
     if not wl.tile_rows:
         wl.tile_rows = (64,)
     dw = DeviceWorkload(wl, tile_rows=wl.tile_rows[0])
