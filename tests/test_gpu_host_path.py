@@ -30,10 +30,13 @@ def _small(kind):
 
 # The host path scores a short first tile (an eighth of a chunk of 1024 rows or more, at
 # most tile_rows) before the rest, in tiles of tile_rows: a tile of 200 rows makes the
-# first tile and every later one start off a multiple of the tile size.
+# first tile and every later one start off a multiple of the tile size. The 4096-row
+# chunk at 128K context is the schedule the benchmark times end to end (a 512-row first
+# tile, seven attention slices).
 @pytest.mark.parametrize("name,copy_stream,tile", [("two_chunks_4098", True, None),
                                                    ("two_chunks_4098", False, None),
                                                    ("two_chunks_4098", True, 200),
+                                                   ("ctx_128k", True, None),
                                                    ("skip_then_full", True, None),
                                                    ("decode", True, None)])
 def test_host_path_equals_device_path(dsa, name, copy_stream, tile):
@@ -49,7 +52,11 @@ def test_host_path_equals_device_path(dsa, name, copy_stream, tile):
     tmax = max(wl.chunks)
     ws = B.PrefillWorkspace(tmax, wl.index_topk, tmax + W - 1, wl.end // wl.ratio,
                             wl.tile_rows[0])
-    st = B.PoolState(wl.end // wl.ratio, "cuda", wl.ratio)
+    if wl.off0:
+        st = B.PoolState.from_prefix(wl.t["prefix_ik"].cuda(), wl.t["prefix_kv"].cuda(),
+                                     wl.off0, wl.end // wl.ratio, "cuda", wl.ratio)
+    else:
+        st = B.PoolState(wl.end // wl.ratio, "cuda", wl.ratio)
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     side = torch.cuda.Stream() if copy_stream else None
     scale = 1.0 / math.sqrt(B.DIM)

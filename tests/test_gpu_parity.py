@@ -350,18 +350,24 @@ def _attn_case(seed, off, T, n, k, window=128, full_sel=False):
     return raw_start, raw, pooled, q, sel
 
 
-@pytest.mark.parametrize("off,T,k", [(0, 67, 16), (1000, 130, 64),
-                                     (5000, 40, 300), (0, 3, 4)])
-def test_attention_matches_oracle(dsa, off, T, k):
+# The window is an argument of the call: besides the model's 128, a single-row window,
+# windows of one row more than a key block (129) and of several blocks (300, 512), some
+# reaching back past token 0.
+@pytest.mark.parametrize("off,T,k,window", [(0, 67, 16, 128), (1000, 130, 64, 128),
+                                            (5000, 40, 300, 128), (0, 3, 4, 128),
+                                            (2000, 50, 64, 1), (700, 33, 16, 129),
+                                            (2000, 70, 64, 300), (100, 40, 8, 512)])
+def test_attention_matches_oracle(dsa, off, T, k, window):
     n = (off + T) // 4
-    raw_start, raw, pooled, q, sel = _attn_case(off + T + k, off, T, n, k)
+    raw_start, raw, pooled, q, sel = _attn_case(off + T + k, off, T, n, k, window)
     out = torch.empty(T, 64, 512, dtype=torch.bfloat16, device="cuda")
     status = torch.zeros(1, dtype=torch.int32, device="cuda")
     B.dsa_window_sparse_attn(q.cuda(), raw.cuda(), raw_start, pooled.cuda(), n,
-                             torch.from_numpy(sel).cuda(), k, T, off, 4, 128, SCALE, out, status)
+                             torch.from_numpy(sel).cuda(), k, T, off, 4, window, SCALE, out,
+                             status)
     torch.cuda.synchronize()
     assert status.item() == 0
-    ref = oracle.attention(q, off + np.arange(T), raw, raw_start, pooled, n, sel, 128, SCALE)
+    ref = oracle.attention(q, off + np.arange(T), raw, raw_start, pooled, n, sel, window, SCALE)
     check_attention(bf16_to_f64(out), ref)
 
 
