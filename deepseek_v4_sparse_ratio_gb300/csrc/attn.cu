@@ -706,6 +706,17 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 const bool live = mbar_wait(o_full, tok & 1, abort_flag, p.status);
                 tc_fence_after();
                 __nv_bfloat16 *orow = p.out + (static_cast<int64_t>(i) * kH + hb) * kD + 32 * sp + lane;
+                // this warp's 32 heads' 1/sum, read once for the four d-tiles (the store loop
+                // is bound by its shared-memory and store instructions)
+                float linv[32];
+#pragma unroll
+                for (int h = 0; h < 32; h += 4) {
+                    const float4 v = *reinterpret_cast<const float4 *>(&sLinv[hb + h]);
+                    linv[h] = v.x;
+                    linv[h + 1] = v.y;
+                    linv[h + 2] = v.z;
+                    linv[h + 3] = v.w;
+                }
 #pragma unroll 1
                 for (int m = 0; m < 4; ++m) {
                     uint32_t oa[32];
@@ -717,7 +728,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                         __nv_bfloat16 *o = orow + 128 * m;
 #pragma unroll
                         for (int h = 0; h < 32; ++h)
-                            o[h * kD] = __float2bfloat16_rn(__uint_as_float(oa[h]) * sLinv[hb + h]);
+                            o[h * kD] = __float2bfloat16_rn(__uint_as_float(oa[h]) * linv[h]);
                     }
                 }
                 tc_fence_before();
