@@ -362,14 +362,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 const uint8_t *src_base =
                     reinterpret_cast<const uint8_t *>(b < x.nwb ? p.raw_kv : p.pooled_kv) + pc * 16;
                 const int par = g & 1;
+                // every group's source row, shuffled once for the block's eight chunks
+                constexpr int kMaxGroups = (32 + kLoadWarps - 1) / kLoadWarps;
+                int srows[kMaxGroups];
+#pragma unroll
+                for (int gq = 0; gq < kMaxGroups; ++gq)
+                    srows[gq] = __shfl_sync(0xFFFFFFFFu, row, (4 * gq + a) & 31);
                 // chunk 7 first, into the slot (usual one for even blocks, spare for odd
                 // ones) of the block two back: this warp already waited for that block's
                 // last PV tile before loading the previous block's chunk 6
 
-#pragma unroll 1
-                for (int gq = 0; gq < ngroups; ++gq) {
+#pragma unroll
+                for (int gq = 0; gq < kMaxGroups; ++gq) {
+                    if (gq >= ngroups) break;
                     const int r = 4 * (lw + kLoadWarps * gq) + a;
-                    const int srow = __shfl_sync(0xFFFFFFFFu, row, 4 * gq + a);
+                    const int srow = srows[gq];
                     const uint8_t *src = src_base + static_cast<int64_t>(srow) * (kD * 2);
                     const uint32_t off = r * 128 + ((pc ^ (r & 7)) << 4);
                     cp_async16((par ? x_base : kv_base + 7 * 16384) + off, src + 7 * 128);
@@ -382,10 +389,11 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     if (lane == 0) ok = mbar_wait(&kv_free[m], (g & 1) ^ 1, abort_flag, p.status);
                     ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
                     if (!ok) break;
-#pragma unroll 1
-                    for (int gq = 0; gq < ngroups; ++gq) {
+#pragma unroll
+                    for (int gq = 0; gq < kMaxGroups; ++gq) {
+                        if (gq >= ngroups) break;
                         const int r = 4 * (lw + kLoadWarps * gq) + a;
-                        const int srow = __shfl_sync(0xFFFFFFFFu, row, 4 * gq + a);
+                        const int srow = srows[gq];
                         const uint8_t *src = src_base + static_cast<int64_t>(srow) * (kD * 2);
                         const uint32_t dst = kv_base + r * 128 + ((pc ^ (r & 7)) << 4);
                         cp_async16(dst + (2 * m) * 16384, src + (2 * m) * 128);
