@@ -24,8 +24,9 @@
 // MN-major by the second, filled and released in chunk pairs (one d-tile of
 // the second MMA each) so the next block's rows stream in while PV drains; a
 // ninth chunk slot takes chunk 7 of odd blocks so that chunk loads ahead.
-// S^T (64 columns) and O^T (4 x 64 columns) live in TMEM. Roles: six loader
-// warps, one warp issuing QK, one issuing PV, eight softmax warps that own
+// S^T (64 columns), O^T (4 x 64 columns) and the running max per head live in
+// TMEM. Roles: six loader warps, one warp issuing QK, one issuing PV, eight
+// softmax warps that own
 // TMEM lanes = keys: they mask, run the online softmax in the log2 domain
 // (exp2 of scale*log2e*logit - running max) and write P^T as bf16. The running
 // max is only raised when some logit exceeds it by more than 8 (log2 units): P
@@ -89,6 +90,11 @@ static_assert(kAttnSmem <= 232448, "over the shared memory of one CTA");
 constexpr uint32_t kLbo7Spare = kOffX - (kOffKV + 6 * 16384);  // chunk 6 -> spare chunk 7
 constexpr uint32_t kSCol = 0;    // S^T: 2 x 64 TMEM columns (double-buffered by block parity)
 constexpr uint32_t kOCol = 256;  // O^T: 4 d-tiles x 64 columns
+// The running max of each head (log2 units), the same in all 128 lanes: 64 columns. A softmax
+// thread loads its 32 heads' maxima together with the block's S^T under one wait, rather
+// than with eight shared-memory loads per block (shared-memory instructions are the scarce
+// issue resource of this kernel: its loaders' copies and the epilogue's stores use them too).
+constexpr uint32_t kMCol = 128;
 constexpr float kRescale = 8.0f;
 
 struct AttnParams {
@@ -354,7 +360,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     last_q = tok;
                 }
             }
-            ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+            // lane 0's result to the warp by a vote (a shuffle would take a shared-memory
+            // instruction slot)
+            ok = (__ballot_sync(0xFFFFFFFFu, ok) & 1u) != 0;
             const int inext = i + istep;
             const TokenInfo xnext = token_info(p, inext < p.T ? inext : i);
             for (int b = crank; b < x.nb && ok; b += kSplit, ++g) {
@@ -387,7 +395,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 // chunk pairs 0-2, then chunk 6, as the previous block's PV releases them
                 for (int m = 0; m < 4 && ok; ++m) {
                     if (lane == 0) ok = mbar_wait(&kv_free[m], (g & 1) ^ 1, abort_flag, p.status);
-                    ok = __shfl_sync(0xFFFFFFFFu, ok, 0);
+                    ok = (__ballot_sync(0xFFFFFFFFu, ok) & 1u) != 0;
                     if (!ok) break;
 #pragma unroll
                     for (int gq = 0; gq < kMaxGroups; ++gq) {
@@ -549,6 +557,13 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
 #pragma unroll
             for (int h = 0; h < 32; ++h) l[h] = 0.0f;
             if (sp == 0) sM[cur * 64 + hb + lane] = -INFINITY;
+            {
+                uint32_t ninf[32];
+#pragma unroll
+                for (int h = 0; h < 32; ++h) ninf[h] = __float_as_uint(-INFINITY);
+                tmem_st32(lane_base + kMCol + hb, ninf);
+                tmem_wait_st();
+            }
             bar_group(hh);
             for (int b = crank; b < x.nb; b += kSplit, ++g) {
                 bool valid;
@@ -564,11 +579,10 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 // and O^T
                 const bool live = mbar_wait(s_full, g & 1, abort_flag, p.status);
                 tc_fence_after();
-                uint32_t sa[32];
-                if (live) {
-                    tmem_ld32(lane_base + kSCol + 64 * (g & 1) + hb, sa);
-                    tmem_wait_ld();
-                }
+                uint32_t sa[32], mv[32];
+                tmem_ld32(lane_base + kMCol + hb, mv);
+                if (live) tmem_ld32(lane_base + kSCol + 64 * (g & 1) + hb, sa);
+                tmem_wait_ld();
                 // this S^T buffer may take the QK of the block after next
                 tc_fence_before();
                 __syncwarp();
@@ -579,15 +593,9 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                 float xv[32];
                 float xmax = -INFINITY;
                 {
-                    const float *m_now = sM + cur * 64 + hb;
 #pragma unroll
-                    for (int h = 0; h < 32; h += 4) {
-                        const float4 m4 = *reinterpret_cast<const float4 *>(&m_now[h]);
-                        xv[h] = fmaf(__uint_as_float(sa[h]), p.c, -m4.x);
-                        xv[h + 1] = fmaf(__uint_as_float(sa[h + 1]), p.c, -m4.y);
-                        xv[h + 2] = fmaf(__uint_as_float(sa[h + 2]), p.c, -m4.z);
-                        xv[h + 3] = fmaf(__uint_as_float(sa[h + 3]), p.c, -m4.w);
-                    }
+                    for (int h = 0; h < 32; ++h)
+                        xv[h] = fmaf(__uint_as_float(sa[h]), p.c, -__uint_as_float(mv[h]));
                     float t16[16];
 #pragma unroll
                     for (int h = 0; h < 16; ++h) t16[h] = fmaxf(xv[h], xv[h + 16]);
@@ -620,9 +628,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
                     const float *m_now = sM + cur * 64 + hb;
 #pragma unroll
                     for (int h = 0; h < 32; ++h) {
+                        mv[h] = __float_as_uint(m_now[h]);
                         l[h] *= sAlpha[hb + h];
                         xv[h] = fmaf(__uint_as_float(sa[h]), p.c, -m_now[h]);
                     }
+                    tmem_st32(lane_base + kMCol + hb, mv);
+                    tmem_wait_st();
                     if (b > crank && live) {
 #pragma unroll 1
                         for (int m = 0; m < 4; ++m) {
