@@ -371,6 +371,26 @@ def test_attention_matches_oracle(dsa, off, T, k, window):
     check_attention(bf16_to_f64(out), ref)
 
 
+# Selections padded with -1 inside the list, so that whole 128-entry key blocks hold no
+# visible key: T = 3 runs the cluster split mode, where such a block is the first one a CTA
+# takes for its token; T = 40 runs one CTA per token, where it follows the window block.
+@pytest.mark.parametrize("T", [3, 40])
+def test_attention_with_empty_key_blocks(dsa, T):
+    off, k = 5000, 1024
+    n = (off + T) // 4
+    raw_start, raw, pooled, q, sel = _attn_case(77 + T, off, T, n, k)
+    sel[:, 256:384] = -1
+    sel[:, 640:768] = -1
+    out = torch.empty(T, 64, 512, dtype=torch.bfloat16, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    B.dsa_window_sparse_attn(q.cuda(), raw.cuda(), raw_start, pooled.cuda(), n,
+                             torch.from_numpy(sel).cuda(), k, T, off, 4, 128, SCALE, out, status)
+    torch.cuda.synchronize()
+    assert status.item() == 0
+    ref = oracle.attention(q, off + np.arange(T), raw, raw_start, pooled, n, sel, 128, SCALE)
+    check_attention(bf16_to_f64(out), ref)
+
+
 def test_attention_reports_bad_index_and_skips_it(dsa):
     off, T, k = 400, 8, 16
     n = (off + T) // 4
