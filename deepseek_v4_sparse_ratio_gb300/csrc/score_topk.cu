@@ -258,8 +258,11 @@ __device__ __forceinline__ void row_range(const RowWalk<NT, U> &rw, int32_t nseg
 // of a higher bin is >= every element of a lower bin).
 struct LinearBins {
     float vmin, scale;
+    // x = (v - vmin) * scale in [0, kBins]; adding 2^23 leaves round(x) in the low bits of
+    // the sum (an FP add and an integer subtract instead of a float-to-int conversion; the
+    // rounding is monotone, which is all the bins need)
     __device__ __forceinline__ int operator()(float v) const {
-        return min(kBins - 1, static_cast<int>((v - vmin) * scale));
+        return min(kBins - 1, __float_as_int(fmaf(v - vmin, scale, 8388608.0f)) - 0x4B000000);
     }
 };
 
@@ -1015,7 +1018,9 @@ __global__ void __launch_bounds__(NT)
         // ---- 2. linear bins between min and max: a monotone map, so every element
         // of a higher bin is >= every element of a lower bin
         const float scale = static_cast<float>(kBins) / (vmax - vmin);
-        auto bin_of = [&](float v) { return min(kBins - 1, static_cast<int>((v - vmin) * scale)); };
+        auto bin_of = [&](float v) {
+            return min(kBins - 1, __float_as_int(fmaf(v - vmin, scale, 8388608.0f)) - 0x4B000000);
+        };
         for (int64_t j = lo + lane; j < hi; j += 32) atomicAdd(&hist[bin_of(src[j])], 1u);
         __syncthreads();
         find_bin<NT>(hist, kBins, static_cast<uint32_t>(k), threadIdx.x, warp_sums, &s_bin,
