@@ -154,18 +154,18 @@ extern "C" int dsa_prefill_chunk_host(dsa_pool_state *st, const dsa_prefill_work
         first = std::min(first, std::max<int64_t>(256, (chunk / 8 + 127) / 128 * 128));
 
     // attention in row slices; each slice's output goes back while the next computes.
-    // The output copy of a row takes about 0.83 of the kernel time of a row, so the
+    // The output copy of a row takes about 0.95 of the kernel time of a row, so the
     // slices shrink towards the end by about that factor (whole waves of one row per
     // SM where possible): the copy left exposed after the last kernel is short and no
     // copy backlog builds up; the first slice is short enough that the output copies
-    // start soon after the selection's. (At 4096 rows and 128K context these seven
-    // slices measured 3.88 ms end to end against 3.98 for five slices of 30, 26, 22, 14
-    // and 8 % of the rows, with the same first score tile.)
+    // start soon after the selection's. (At 4096 rows and 128K context these eight
+    // slices measured 3.612 ms end to end against 3.652 for seven slices of 22, 19, 18,
+    // 15, 11, 8 and 7 % of the rows.)
     int64_t cuts[8];
     int ncut = 0;
     {
         const int64_t waves = (chunk + sms - 1) / sms;
-        static const double kCum[] = {0.22, 0.41, 0.59, 0.74, 0.85, 0.93};
+        static const double kCum[] = {0.185, 0.333, 0.481, 0.630, 0.741, 0.852, 0.926};
         if (chunk >= 1024) {
             for (double f : kCum) {
                 const int64_t r = static_cast<int64_t>(f * static_cast<double>(waves) + 0.5) * sms;

@@ -270,7 +270,7 @@ typedef struct dsa_prefill_workspace {
  *   rows) are copied on `stream`, the other indexer query rows and then the
  *   query rows on copy_stream while the pooling and indexer run; the later
  *   score tiles wait for their rows; the selection of the first tile is copied
- *   back while the later tiles score; the attention runs in up to seven row
+ *   back while the later tiles score; the attention runs in up to eight row
  *   slices of shrinking size and each slice's output is copied back on
  *   copy_stream while the next slice computes. When `stream`
  *   completes, every copy has completed and the host outputs are valid.

@@ -32,7 +32,7 @@ def _small(kind):
 # most tile_rows) before the rest, in tiles of tile_rows: a tile of 200 rows makes the
 # first tile and every later one start off a multiple of the tile size. The 4096-row
 # chunk at 128K context is the schedule the benchmark times end to end (a 512-row first
-# tile, seven attention slices).
+# tile, eight attention slices).
 @pytest.mark.parametrize("name,copy_stream,tile", [("two_chunks_4098", True, None),
                                                    ("two_chunks_4098", False, None),
                                                    ("two_chunks_4098", True, 200),
