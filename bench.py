@@ -97,12 +97,12 @@ def score_scratch_bytes(wl, tile):
 NCU_TRAFFIC = {
     "attn_kernel": {"bytes": 343.973e6 + 234.555e6, "files": ("attn.cu", "common.cuh", "internal.h"),
                     "sha256_16": "22b9450e9f54fa85"},
-    "score_kernel": {"bytes": 76.969e6 + 476.884e6,
+    "score_kernel": {"bytes": 77.502e6 + 477.237e6,
                      "files": ("score_topk.cu", "common.cuh", "internal.h"),
-                     "sha256_16": "51dd0570c634929a"},
-    "topk_kernel": {"bytes": 692.426e6 + 30.576e6,
+                     "sha256_16": "66d381207997d1e8"},
+    "topk_kernel": {"bytes": 685.981e6 + 30.818e6,
                     "files": ("score_topk.cu", "common.cuh", "internal.h"),
-                    "sha256_16": "51dd0570c634929a"},
+                    "sha256_16": "66d381207997d1e8"},
 }
 
 
