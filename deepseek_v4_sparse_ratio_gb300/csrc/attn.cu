@@ -25,10 +25,10 @@
 // the second MMA each) so the next block's rows stream in while PV drains; a
 // ninth chunk slot takes chunk 7 of odd blocks so that chunk loads ahead.
 // S^T (64 columns), O^T (4 x 64 columns) and the running max per head live in
-// TMEM. Roles: six loader warps, one warp issuing QK, one issuing PV, eight
-// softmax warps that own
-// TMEM lanes = keys: they mask, run the online softmax in the log2 domain
-// (exp2 of scale*log2e*logit - running max) and write P^T as bf16. The running
+// TMEM. Roles: six loader warps (key rows), one warp loading Q and issuing QK,
+// one issuing PV, eight softmax warps that own TMEM lanes = keys: they mask,
+// run the online softmax in the log2 domain (exp2 of scale*log2e*logit -
+// running max) and write P^T as bf16. The running
 // max is only raised when some logit exceeds it by more than 8 (log2 units): P
 // then stays <= 256, and the rescale of O^T and of the partial sums is skipped
 // on most blocks without changing the result (the same max divides out at the
@@ -316,13 +316,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
       // instance for all eight warps)
       asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegsLow));
       if (warp < kLoadWarps) {
-        // ---------------- loaders: Q by TMA (warp 0, lane 0); key rows by cp.async, 8
+        // ---------------- loaders: key rows by cp.async (the QK warp loads Q), 8
         // lanes per 128-byte row piece, written straight into the 128-byte-swizzled tile.
         // Loader lw copies the 4-row groups lw, lw+6, lw+12, ... (at most 6, 24 rows).
         // Each block's selection entries are read one block ahead.
         DSA_SPLIT_COORDS
         const int lw = warp;
-        const uint64_t pol_stream = policy_evict_first();
         const uint32_t kv_base = smem_u32(sKV);
         const uint32_t x_base = smem_u32(smem + kOffX);
         const int a = lane >> 3, pc = lane & 7;
@@ -345,24 +344,12 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
             if (holder && !valid && j != -1 && pos < x.nsel) report(p.status, DSA_ERR_BOUNDS);
             return valid ? j : 0;
         };
-        int tok = 0, g = 0, last_q = -1;
+        int tok = 0, g = 0;
         bool ok = true;
         int i = i0;
         TokenInfo x = token_info(p, i < p.T ? i : 0);
         int32_t jn = i < p.T ? fetch(x, i, crank) : -1;
         for (; i < p.T && ok; i += istep, ++tok) {
-            if (lw == 0 && lane == 0) {
-                ok = mbar_wait(q_free, (tok & 1) ^ 1, abort_flag, p.status);
-                if (ok) {
-                    mbar_expect_tx(q_full, 65536);
-                    for (int c = 0; c < 8; ++c)
-                        tma_load_2d(sQ + c * 8192, &tm_q, q_full, c * 64, i * 64, pol_stream);
-                    last_q = tok;
-                }
-            }
-            // lane 0's result to the warp by a vote (a shuffle would take a shared-memory
-            // instruction slot)
-            ok = (__ballot_sync(0xFFFFFFFFu, ok) & 1u) != 0;
             const int inext = i + istep;
             const TokenInfo xnext = token_info(p, inext < p.T ? inext : i);
             for (int b = crank; b < x.nb && ok; b += kSplit, ++g) {
@@ -414,7 +401,7 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         // no copy into this CTA's shared memory may still be in flight at exit
         asm volatile("cp.async.wait_all;" ::: "memory");
-        if (lw == 0 && lane == 0 && last_q >= 0) drain_wait(q_full, last_q & 1);
+
         __syncwarp();
         if constexpr (kSplit > 1) {
             // the three cluster barriers of the softmax warps' merge
@@ -432,10 +419,21 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         const uint64_t ad0 = desc_sw128(smem_u32(sKV), 16, 1024);
         const uint64_t adx = desc_sw128(smem_u32(smem + kOffX), 16, 1024);
         const uint64_t bd0 = desc_sw128(smem_u32(sQ), 16, 1024);
-        int tok = 0, g = 0;
+        const uint64_t pol_stream = policy_evict_first();
+        int tok = 0, g = 0, last_q = -1;
         bool ok = true;
         for (int i = i0; i < p.T && ok; i += istep, ++tok) {
             const TokenInfo x = token_info(p, i);
+            // this token's queries: this warp's own QK of the previous token has read Q
+            // (q_free), so the copy goes out as soon as that completes, without waiting for
+            // the loaders
+            if (!(ok = mbar_wait(q_free, (tok & 1) ^ 1, abort_flag, p.status))) break;
+            if (leader) {
+                mbar_expect_tx(q_full, 65536);
+                for (int c = 0; c < 8; ++c)
+                    tma_load_2d(sQ + c * 8192, &tm_q, q_full, c * 64, i * 64, pol_stream);
+            }
+            last_q = tok;
             if (!(ok = mbar_wait(q_full, tok & 1, abort_flag, p.status))) break;
             tc_fence_after();
             for (int b = crank; b < x.nb && ok; b += kSplit, ++g) {
@@ -483,6 +481,8 @@ __global__ void __launch_bounds__(kAttnThreads, 1)
         }
         mma_commit_if(&drain[0], leader);
         if (leader) drain_wait(&drain[0], 0);
+        // no copy into this CTA's shared memory may still be in flight at exit
+        if (leader && last_q >= 0) drain_wait(q_full, last_q & 1);
         __syncwarp();
         if constexpr (kSplit > 1) {
             cluster_sync();
