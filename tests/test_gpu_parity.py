@@ -352,11 +352,14 @@ def _attn_case(seed, off, T, n, k, window=128, full_sel=False):
 
 # The window is an argument of the call: besides the model's 128, a single-row window,
 # windows of one row more than a key block (129) and of several blocks (300, 512), some
-# reaching back past token 0.
+# reaching back past token 0. The last two cases have more tokens than twice the SM count,
+# so each persistent CTA takes several tokens in turn (the query reload between tokens, and
+# the barrier phases carried across tokens of one, two and three key blocks).
 @pytest.mark.parametrize("off,T,k,window", [(0, 67, 16, 128), (1000, 130, 64, 128),
                                             (5000, 40, 300, 128), (0, 3, 4, 128),
                                             (2000, 50, 64, 1), (700, 33, 16, 129),
-                                            (2000, 70, 64, 300), (100, 40, 8, 512)])
+                                            (2000, 70, 64, 300), (100, 40, 8, 512),
+                                            (0, 700, 64, 128), (20000, 400, 256, 128)])
 def test_attention_matches_oracle(dsa, off, T, k, window):
     n = (off + T) // 4
     raw_start, raw, pooled, q, sel = _attn_case(off + T + k, off, T, n, k, window)
