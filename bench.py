@@ -97,12 +97,12 @@ def score_scratch_bytes(wl, tile):
 NCU_TRAFFIC = {
     "attn_kernel": {"bytes": 344.883e6 + 234.731e6, "files": ("attn.cu", "common.cuh", "internal.h"),
                     "sha256_16": "ad8d44af46bd578c"},
-    "score_kernel": {"bytes": 77.502e6 + 477.237e6,
+    "score_kernel": {"bytes": 76.964e6 + 477.065e6,
                      "files": ("score_topk.cu", "common.cuh", "internal.h"),
-                     "sha256_16": "66d381207997d1e8"},
-    "topk_kernel": {"bytes": 685.981e6 + 30.818e6,
+                     "sha256_16": "eafc9258000d2b8f"},
+    "topk_kernel": {"bytes": 683.301e6 + 31.162e6,
                     "files": ("score_topk.cu", "common.cuh", "internal.h"),
-                    "sha256_16": "66d381207997d1e8"},
+                    "sha256_16": "eafc9258000d2b8f"},
 }
 
 
