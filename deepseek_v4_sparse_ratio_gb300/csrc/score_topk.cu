@@ -668,12 +668,18 @@ __device__ __forceinline__ void drain_wait(uint64_t *bar, uint32_t parity) {
         if (clock64() - t0 > kWaitBudget) break;
 }
 
-// Stores the masked score of (row, pooled row j) and returns it (-inf when masked
-// or when the row is past the tile).
-__device__ __forceinline__ float store_score(const ScoreParams &p, int row, int64_t j, float acc) {
-    if (row >= p.R) return -INFINITY;
+// Visible pooled rows of tile row `row` (0 past the tile).
+__device__ __forceinline__ int64_t row_nvis(const ScoreParams &p, int row) {
+    if (row >= p.R) return 0;
     const int64_t t = p.offset + p.r0 + row;
-    const int64_t nv = min(p.n, (t + 1) / p.ratio);
+    return min(p.n, (t + 1) / p.ratio);
+}
+
+// Stores the masked score of (row, pooled row j) and returns it (-inf when masked
+// or when the row is past the tile); nv = row_nvis(p, row), computed once per unit.
+__device__ __forceinline__ float store_score(const ScoreParams &p, int row, int64_t nv, int64_t j,
+                                             float acc) {
+    if (row >= p.R) return -INFINITY;
     // sum of (+0) and (-0) terms can be -0; keep one zero so key order is total
     const float s = j < nv ? (acc == 0.0f ? 0.0f : acc) : -INFINITY;
     __stcs(p.scores + static_cast<int64_t>(row) * p.stride + j, s);
@@ -827,6 +833,9 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
             }
             asm volatile("bar.sync 1, %0;" ::"r"(nthr) : "memory");
             bool ok = !*abort_flag;
+            // once per unit: the compiler left this 64-bit division inside the key-block
+            // loop (score + top-k at 128K 1.566 against 1.606 ms with it there)
+            const int64_t nv0 = row_nvis(p, x.row0 + tl), nv1 = row_nvis(p, x.row0 + 4 + tl);
             // range of the visible scores of this warp's two rows (half 0 / 1)
             float rmin0 = INFINITY, rmax0 = -INFINITY, rmin1 = INFINITY, rmax1 = -INFINITY;
             for (int kb = x.b0; kb < x.b1 && ok; ++kb) {
@@ -883,7 +892,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                         }
                         float ae, ao;
                         asm("mov.b64 {%0, %1}, %2;" : "=f"(ae), "=f"(ao) : "l"(acc));
-                        const float sc = store_score(p, x.row0 + ti, j, ae + ao);
+                        const float sc = store_score(p, x.row0 + ti, half ? nv1 : nv0, j, ae + ao);
                         const float sv = sc == -INFINITY ? INFINITY : sc;
                         if (half) {
                             rmin1 = fminf(rmin1, sv);
@@ -895,7 +904,7 @@ __global__ void __launch_bounds__(kScoreThreads, 1)
                     }
                 } else {
                     for (int half = 0; half < 2; ++half)
-                        store_score(p, x.row0 + half * 4 + tl, j, -INFINITY);
+                        store_score(p, x.row0 + half * 4 + tl, half ? nv1 : nv0, j, -INFINITY);
                 }
             }
             if (p.rng) {
