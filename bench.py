@@ -97,12 +97,12 @@ def score_scratch_bytes(wl, tile):
 NCU_TRAFFIC = {
     "attn_kernel": {"bytes": 344.883e6 + 234.731e6, "files": ("attn.cu", "common.cuh", "internal.h"),
                     "sha256_16": "ad8d44af46bd578c"},
-    "score_kernel": {"bytes": 76.958e6 + 477.148e6,
+    "score_kernel": {"bytes": 77.047e6 + 477.075e6,
                      "files": ("score_topk.cu", "common.cuh", "internal.h"),
-                     "sha256_16": "12da10154b2cc305"},
-    "topk_kernel": {"bytes": 750.793e6 + 31.106e6,
+                     "sha256_16": "aee7f2220c43dae9"},
+    "topk_kernel": {"bytes": 754.475e6 + 31.134e6,
                     "files": ("score_topk.cu", "common.cuh", "internal.h"),
-                    "sha256_16": "12da10154b2cc305"},
+                    "sha256_16": "aee7f2220c43dae9"},
 }
 
 
