@@ -266,6 +266,11 @@ struct LinearBins {
     }
 };
 
+// The float whose order key is u (the inverse of order_key).
+__device__ __forceinline__ float key_float(uint32_t u) {
+    return __uint_as_float((u & 0x80000000u) ? (u ^ 0x80000000u) : ~u);
+}
+
 // Emission in index order: kept element j goes to (#above-threshold before j) +
 // min(#equal before j, need_eq); w_gt / w_eq hold each warp segment's counts.
 template <int NT, int U>
@@ -1151,10 +1156,14 @@ __global__ void __launch_bounds__(NT)
         base_eq += w_eq[w];
     }
     const uint32_t lt_mask = (1u << lane) - 1u;
-    auto emit = [&](int64_t base, uint32_t u) {
+    // the scores hold no -0 (stored as +0) and no NaN, so comparing the values orders
+    // them exactly as their keys do (one compare per score instead of its key: score +
+    // top-k at 128K 1.554 against 1.566 ms)
+    const float t_val = key_float(thr);
+    auto emit = [&](int64_t base, float v) {
         const int64_t j = base + lane;
-        const bool gt = j < hi && u > thr;
-        const bool eq = j < hi && u == thr;
+        const bool gt = j < hi && v > t_val;
+        const bool eq = j < hi && v == t_val;
         const uint32_t mg = __ballot_sync(0xFFFFFFFFu, gt);
         const uint32_t me = __ballot_sync(0xFFFFFFFFu, eq);
         const uint32_t eq_before = base_eq + __popc(me & lt_mask);
@@ -1171,12 +1180,11 @@ __global__ void __launch_bounds__(NT)
             for (int q = 0; q < 7; ++q) v[q] = src[base + 32 * q + lane];
             v[7] = base + 224 + lane < hi ? src[base + 224 + lane] : 0.0f;
 #pragma unroll
-            for (int q = 0; q < 7; ++q) emit(base + 32 * q, order_key(v[q]));
-            emit(base + 224, base + 224 + lane < hi ? order_key(v[7]) : 0u);
+            for (int q = 0; q < 8; ++q) emit(base + 32 * q, v[q]);
         }
         for (; base < hi; base += 32) {
             const int64_t j = base + lane;
-            emit(base, j < hi ? order_key(src[j]) : 0u);
+            emit(base, j < hi ? src[j] : 0.0f);
         }
     }
 }
