@@ -97,12 +97,12 @@ def score_scratch_bytes(wl, tile):
 NCU_TRAFFIC = {
     "attn_kernel": {"bytes": 344.883e6 + 234.731e6, "files": ("attn.cu", "common.cuh", "internal.h"),
                     "sha256_16": "ad8d44af46bd578c"},
-    "score_kernel": {"bytes": 77.047e6 + 477.075e6,
+    "score_kernel": {"bytes": 77.305e6 + 477.479e6,
                      "files": ("score_topk.cu", "common.cuh", "internal.h"),
-                     "sha256_16": "aee7f2220c43dae9"},
-    "topk_kernel": {"bytes": 754.475e6 + 31.134e6,
+                     "sha256_16": "7ba956ee17a05555"},
+    "topk_kernel": {"bytes": 747.595e6 + 30.609e6,
                     "files": ("score_topk.cu", "common.cuh", "internal.h"),
-                    "sha256_16": "aee7f2220c43dae9"},
+                    "sha256_16": "7ba956ee17a05555"},
 }
 
 
