@@ -96,7 +96,7 @@ def score_scratch_bytes(wl, tile):
 # the sources the captured build came from; a changed source reports null.
 NCU_TRAFFIC = {
     "attn_kernel": {"bytes": 344.883e6 + 234.731e6, "files": ("attn.cu", "common.cuh", "internal.h"),
-                    "sha256_16": "ad8d44af46bd578c"},
+                    "sha256_16": "babec7cc87d7dd59"},
     "score_kernel": {"bytes": 77.305e6 + 477.479e6,
                      "files": ("score_topk.cu", "common.cuh", "internal.h"),
                      "sha256_16": "7ba956ee17a05555"},

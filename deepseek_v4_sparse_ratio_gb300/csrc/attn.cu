@@ -28,12 +28,12 @@
 // TMEM. Roles: six loader warps (key rows), one warp loading Q and issuing QK,
 // one issuing PV, eight softmax warps that own TMEM lanes = keys: they mask,
 // run the online softmax in the log2 domain (exp2 of scale*log2e*logit -
-// running max) and write P^T as bf16. The running
-// max is only raised when some logit exceeds it by more than 8 (log2 units): P
-// then stays <= 256, and the rescale of O^T and of the partial sums is skipped
-// on most blocks without changing the result (the same max divides out at the
-// end). Output = O^T / sum, bf16, stored by the softmax warps straight from the
-// registers they read O^T into.
+// running max) and write P^T as bf16. The running max is only raised when some
+// logit exceeds it by more than 8 (log2 units): P then stays <= 256, and the
+// rescale of O^T and of the partial sums is skipped on most blocks without
+// changing the result (the same max divides out at the end). Output =
+// O^T / sum, bf16, stored by the softmax warps straight from the registers they
+// read O^T into.
 //
 // Few tokens (decode steps, short bands): one CTA per token would leave most SMs
 // idle while it walks the token's blocks in sequence, so a cluster of 8 CTAs
