@@ -1283,12 +1283,16 @@ __global__ void __launch_bounds__(256) fill_selection_kernel(int32_t *sel, int32
 int choose_segments(int groups, int NB, int sms) {
     int best = 1;
     double best_cost = 1e30;
-    // (up to 32 segments; more when the row groups alone leave SMs idle)
+    // (up to 32 segments; more when the row groups alone leave SMs idle). A unit costs
+    // its key blocks plus about two blocks' time of start-up (its queries' load); with 4
+    // the 4096-row 128K tile took two segments per row group (7 waves of 1,024 units, the
+    // last one 74 % full), with 2 it takes five (17 waves, 99 % full): score + top-k 1.502
+    // against 1.535 ms, the 1M tiles unchanged
     const int cap = std::min(NB, std::max(32, sms / std::max(1, groups)));
     for (int ns = 1; ns <= cap; ++ns) {
         const int64_t units = static_cast<int64_t>(groups) * ns;
         const int64_t waves = (units + sms - 1) / sms;
-        const double cost = static_cast<double>(waves) * (static_cast<double>(NB) / ns + 4.0);
+        const double cost = static_cast<double>(waves) * (static_cast<double>(NB) / ns + 2.0);
         if (cost < best_cost * 0.999) {
             best_cost = cost;
             best = ns;
