@@ -97,12 +97,12 @@ def score_scratch_bytes(wl, tile):
 NCU_TRAFFIC = {
     "attn_kernel": {"bytes": 344.883e6 + 234.731e6, "files": ("attn.cu", "common.cuh", "internal.h"),
                     "sha256_16": "babec7cc87d7dd59"},
-    "score_kernel": {"bytes": 76.786e6 + 477.784e6,
+    "score_kernel": {"bytes": 76.964e6 + 478.236e6,
                      "files": ("score_topk.cu", "common.cuh", "internal.h"),
-                     "sha256_16": "118440dba360da73"},
-    "topk_kernel": {"bytes": 753.388e6 + 30.600e6,
+                     "sha256_16": "0abc06343f652829"},
+    "topk_kernel": {"bytes": 627.258e6 + 28.559e6,
                     "files": ("score_topk.cu", "common.cuh", "internal.h"),
-                    "sha256_16": "118440dba360da73"},
+                    "sha256_16": "0abc06343f652829"},
 }
 
 
