@@ -150,7 +150,10 @@ def test_topk_ties_break_toward_lower_index(dsa):
 
 @pytest.mark.parametrize("L,m,k,T", [(4000, 100, 64, 4), (4000, 100, 64, 320),
                                      (4000, 600, 300, 4), (4000, 600, 300, 320),
-                                     (4000, 100, 3000, 320), (70000, 100, 64, 320),
+                                     (4000, 100, 3000, 320), (20000, 100, 64, 4),
+                                     (20000, 100, 64, 320), (20000, 600, 300, 4),
+                                     (20000, 600, 300, 320), (20000, 100, 1000, 320),
+                                     (20000, 100, 3000, 320), (70000, 100, 64, 320),
                                      (70000, 3000, 2048, 4)])
 def test_topk_heavy_ties_on_every_selection_path(dsa, L, m, k, T):
     """m pooled rows are one repeated key aligned with every indexer query, so m
@@ -160,8 +163,11 @@ def test_topk_heavy_ties_on_every_selection_path(dsa, L, m, k, T):
     cover every way the top-k finds its threshold: a few candidates ranked
     against each other, a crowded threshold bin (radix select over the
     candidates), and a bin too crowded to collect (radix select over the row),
-    on rows of 4,000 and of 70,000 scores, in tiles of 4 rows (1024-thread
-    CTAs) and of 320 rows (256-thread CTAs). Ties must go to the lowest
+    on rows of 4,000, 20,000 and 70,000 scores, in tiles of 4 rows (1024-thread
+    CTAs) and of 320 rows (256-thread CTAs). Rows of 20,000 emit from the kept-
+    index bitmap when the candidates were ranked against each other (the cut
+    inside the repeated group keeps its lowest indices there) and fall back to
+    the ordered pass after a radix select. Ties must go to the lowest
     indices."""
     g = torch.Generator().manual_seed(L + m + k)
     off = 4 * L
