@@ -99,10 +99,10 @@ NCU_TRAFFIC = {
                     "sha256_16": "babec7cc87d7dd59"},
     "score_kernel": {"bytes": 76.964e6 + 478.236e6,
                      "files": ("score_topk.cu", "common.cuh", "internal.h"),
-                     "sha256_16": "0abc06343f652829"},
+                     "sha256_16": "0d66d1fb771e9c91"},
     "topk_kernel": {"bytes": 627.258e6 + 28.559e6,
                     "files": ("score_topk.cu", "common.cuh", "internal.h"),
-                    "sha256_16": "0abc06343f652829"},
+                    "sha256_16": "0d66d1fb771e9c91"},
 }
 
 

@@ -970,8 +970,10 @@ constexpr int kTopkThreadsFew = 1024;
 constexpr int kTopkThreadsLong = 512;   // persistent CTAs for rows over 64K scores
 
 // One CTA per query row; every pass walks the row in per-warp contiguous
-// segments (coalesced, and the last pass must emit in index order). Rows are
-// taken last first: the score kernel writes the last rows last, so theirs are
+// segments (coalesced, and an ordered last pass emits in index order). With BM,
+// rows of kBitmapRows to 32 x kBins scores skip that pass: the kept scores are
+// marked in a bitmap while the candidates are collected, and the indices are
+// written from it. Rows are taken last first: the score kernel writes the last rows last, so theirs are
 // the scores still in L2. With nseg > 0 the row's range comes from the score
 // kernel (segment s's min and max in the row's selection entries 2s, 2s+1).
 template <int NT, bool BM>
